@@ -1,0 +1,405 @@
+/*
+ * pkv_oracle.c -- plain fp64 CPU oracle for attention over a paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the bench's CPU-baseline
+ * leg use it.  It shares no code, header, table or helper with the CUDA
+ * library; it takes the same raw input arrays and nothing else.
+ *
+ * What it computes, and where the pages state it (TileInfer.jl "Performance"
+ * page, section "Fused kernels, FlashAttention and PagedAttention", and the
+ * "INT8 KV cache" section of the same page):
+ *
+ *  - The reference ("ref") attention path gathers the pool pages named by the
+ *    block table into dense K and V and materialises the scores; the paged
+ *    flash kernels compute the same softmax attention, only online and in
+ *    place.  So the oracle is the plain definition: gather, score, softmax
+ *    (two passes: max, then sum), weighted sum of V.  orc_paged_attention.
+ *  - Split-KV decode writes one partial per split and a separate combine
+ *    kernel merges them (same section, the "Not kept" note on the fused
+ *    combine).  orc_paged_attention with num_splits > 0 restates that:
+ *    partial softmax per position range plus a log-sum-exp merge.
+ *  - The INT8 cache keeps one scale per cached vector, keys smoothed by the
+ *    key norm's weight ("INT8 KV cache" section).  orc_quantize_row_int8 and
+ *    orc_kv_append_int8 follow the reading: x = float(k) (divided by w when
+ *    smoothing), scale = max|x| / 127 in fp32, code = round-half-even of the
+ *    fp32 quotient x / scale, clamped to [-127, 127]; an all-zero vector gets
+ *    scale 0 and codes 0.
+ *  - The KV write copies the new K/V vectors into the pages named by the
+ *    block table (same page, list of fused kernels, "the KV cache write").
+ *    orc_kv_append_bf16.
+ *
+ * Readings where the pages are silent:
+ *  - Causal alignment is bottom-right: query row i of a sequence with q_b new
+ *    rows and L_b cached positions (new rows included) sits at absolute
+ *    position L_b - q_b + i and sees keys 0 .. L_b - q_b + i.
+ *  - GQA grouping is consecutive: query head h uses KV head h / (Hq / Hkv).
+ *  - lse is the natural log of sum_j exp(scale * q.k_j).
+ *  - An empty visible set gives out = 0 and lse = -inf.
+ *
+ * Pool layout (one pool each for K and V): [num_pages][Hkv][page_size][D];
+ * bf16 entries are raw 16-bit patterns, int8 entries carry an fp32 scale per
+ * (page, head, slot) in [num_pages][Hkv][page_size].  Position p of sequence
+ * b lives in page block_table[b][p / page_size], slot p % page_size.
+ *
+ * Arithmetic is fp64 except the quantiser, which the reading fixes to fp32.
+ * Build without fast-math and with -ffp-contract=off so both the x86 and the
+ * Arm host give the same bits.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORC_BF16 0
+#define ORC_INT8 1
+
+typedef struct {
+  const void* k;            /* bf16 bits (uint16) or int8 codes */
+  const void* v;
+  const float* k_scale;     /* int8 only: [num_pages][Hkv][page_size] */
+  const float* v_scale;
+  const float* k_smooth;    /* int8 only, optional: [D] per-channel key weight */
+  int num_pages, num_kv_heads, page_size, head_dim, dtype;
+} orc_pool;
+
+static double bf16_bits_to_double(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+static float bf16_bits_to_float(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Index of element c of position p of sequence b, KV head h, in the pool. */
+static size_t pool_index(const orc_pool* pl, const int32_t* bt_row, int p, int h, int c) {
+  int page = bt_row[p / pl->page_size];
+  int slot = p % pl->page_size;
+  return (((size_t)page * pl->num_kv_heads + h) * pl->page_size + slot) * pl->head_dim + c;
+}
+
+static size_t scale_index(const orc_pool* pl, const int32_t* bt_row, int p, int h) {
+  int page = bt_row[p / pl->page_size];
+  int slot = p % pl->page_size;
+  return ((size_t)page * pl->num_kv_heads + h) * pl->page_size + slot;
+}
+
+/* Dequantised K[p][c] of KV head h (fp64). */
+static double key_at(const orc_pool* pl, const int32_t* bt_row, int p, int h, int c) {
+  size_t i = pool_index(pl, bt_row, p, h, c);
+  if (pl->dtype == ORC_BF16) return bf16_bits_to_double(((const uint16_t*)pl->k)[i]);
+  double code = (double)((const int8_t*)pl->k)[i];
+  double s = (double)pl->k_scale[scale_index(pl, bt_row, p, h)];
+  double w = pl->k_smooth ? (double)pl->k_smooth[c] : 1.0;
+  return code * s * w;
+}
+
+static double value_at(const orc_pool* pl, const int32_t* bt_row, int p, int h, int c) {
+  size_t i = pool_index(pl, bt_row, p, h, c);
+  if (pl->dtype == ORC_BF16) return bf16_bits_to_double(((const uint16_t*)pl->v)[i]);
+  double code = (double)((const int8_t*)pl->v)[i];
+  return code * (double)pl->v_scale[scale_index(pl, bt_row, p, h)];
+}
+
+/*
+ * Softmax attention of one query vector q (fp64, length D) over positions
+ * [lo, hi) of one sequence and KV head, two passes: max, then sum.  Writes
+ * the normalised output o[D] and returns lse = m + ln(sum exp(s - m)).
+ * An empty range gives o = 0 and lse = -inf.
+ */
+static double attend_range(const orc_pool* pl, const int32_t* bt_row, int h_kv,
+                           const double* q, double scale, int lo, int hi,
+                           double* s_buf, double* o) {
+  const int D = pl->head_dim;
+  for (int c = 0; c < D; ++c) o[c] = 0.0;
+  if (hi <= lo) return -INFINITY;
+  double m = -INFINITY;
+  for (int p = lo; p < hi; ++p) {
+    double dot = 0.0;
+    for (int c = 0; c < D; ++c) dot += q[c] * key_at(pl, bt_row, p, h_kv, c);
+    s_buf[p - lo] = scale * dot;
+    if (s_buf[p - lo] > m) m = s_buf[p - lo];
+  }
+  double sum = 0.0;
+  for (int p = lo; p < hi; ++p) sum += exp(s_buf[p - lo] - m);
+  double lse = m + log(sum);
+  for (int p = lo; p < hi; ++p) {
+    double w = exp(s_buf[p - lo] - lse);
+    for (int c = 0; c < D; ++c) o[c] += w * value_at(pl, bt_row, p, h_kv, c);
+  }
+  return lse;
+}
+
+/* ---------------------------------------------------------------- threads */
+
+typedef struct {
+  void (*fn)(void* ctx, long task, double* scratch);
+  void* ctx;
+  long ntasks;
+  long next;            /* shared task counter (gcc atomics) */
+  size_t scratch_len;   /* doubles of per-thread scratch */
+} task_pool;
+
+static void* worker(void* arg) {
+  task_pool* tp = (task_pool*)arg;
+  double* scratch = (double*)malloc(tp->scratch_len * sizeof(double));
+  if (!scratch) return (void*)1;
+  for (;;) {
+    long t = __atomic_fetch_add(&tp->next, 1, __ATOMIC_RELAXED);
+    if (t >= tp->ntasks) break;
+    tp->fn(tp->ctx, t, scratch);
+  }
+  free(scratch);
+  return NULL;
+}
+
+static int run_tasks(void (*fn)(void*, long, double*), void* ctx, long ntasks,
+                     size_t scratch_len, int nthreads) {
+  if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > ntasks) nthreads = (int)(ntasks > 0 ? ntasks : 1);
+  task_pool tp = {fn, ctx, ntasks, 0, scratch_len};
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  if (!th) return -1;
+  int started = 0, rc = 0;
+  for (int i = 0; i < nthreads; ++i) {
+    if (pthread_create(&th[i], NULL, worker, &tp) != 0) { rc = -1; break; }
+    ++started;
+  }
+  if (started == 0) rc = (worker(&tp) == NULL) ? 0 : -1;
+  for (int i = 0; i < started; ++i) {
+    void* r = NULL;
+    pthread_join(th[i], &r);
+    if (r) rc = -1;
+  }
+  free(th);
+  return rc;
+}
+
+/* --------------------------------------------------------- attention rows */
+
+typedef struct {
+  const orc_pool* pool;
+  const uint16_t* q;        /* bf16 bits [total_q][Hq][D] */
+  const int32_t* cu_q;      /* [B+1] */
+  int B, Hq;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  double scale;
+  const int32_t* rows;      /* query rows (indices into total_q) to evaluate */
+  int num_splits;           /* 0: unsplit; >0: split-KV partials + combine */
+  double* out;              /* [nrows][Hq][D] */
+  double* lse;              /* [nrows][Hq] */
+  int status;
+} attn_ctx;
+
+/* Sequence that owns query row r: the b with cu_q[b] <= r < cu_q[b+1]. */
+static int owner_sequence(const int32_t* cu_q, int B, int r) {
+  for (int b = 0; b < B; ++b)
+    if (r >= cu_q[b] && r < cu_q[b + 1]) return b;
+  return -1;
+}
+
+static void attn_task(void* vctx, long task, double* scratch) {
+  attn_ctx* a = (attn_ctx*)vctx;
+  const orc_pool* pl = a->pool;
+  const int D = pl->head_dim;
+  const int G = a->Hq / pl->num_kv_heads;
+  long ri = task / a->Hq;
+  int hq = (int)(task % a->Hq);
+  int r = a->rows[ri];
+  int b = owner_sequence(a->cu_q, a->B, r);
+  if (b < 0) { a->status = -1; return; }
+  int qlen = a->cu_q[b + 1] - a->cu_q[b];
+  int L = a->seq_lens[b];
+  int pos = L - qlen + (r - a->cu_q[b]);   /* bottom-right causal position */
+  int visible = pos + 1;                    /* keys 0..pos */
+  if (visible > L) visible = L;
+  if (visible < 0) visible = 0;
+  const int32_t* bt_row = a->block_table + (size_t)b * a->max_pages;
+  int h_kv = hq / G;
+
+  double* qd = scratch;               /* D */
+  double* o = scratch + D;            /* D */
+  double* opart = scratch + 2 * D;    /* D */
+  double* s_buf = scratch + 3 * D;    /* up to L */
+  for (int c = 0; c < D; ++c)
+    qd[c] = bf16_bits_to_double(a->q[((size_t)r * a->Hq + hq) * D + c]);
+
+  double* out = a->out + ((size_t)ri * a->Hq + hq) * D;
+  double lse;
+  if (a->num_splits <= 0) {
+    lse = attend_range(pl, bt_row, h_kv, qd, a->scale, 0, visible, s_buf, o);
+    for (int c = 0; c < D; ++c) out[c] = o[c];
+  } else {
+    /* Split-KV: split sigma covers positions [sigma*C, min((sigma+1)*C, n)),
+     * C = ceil(n / S).  Each split yields a normalised partial and its lse;
+     * the combine weighs partial sigma by exp(lse_sigma - lse) with
+     * lse = ln sum_sigma exp(lse_sigma).  Empty splits have lse = -inf. */
+    int S = a->num_splits;
+    int C = (visible + S - 1) / S;
+    double* lse_part = (double*)malloc(sizeof(double) * (size_t)S);
+    double* o_part = (double*)malloc(sizeof(double) * (size_t)S * D);
+    if (!lse_part || !o_part) { free(lse_part); free(o_part); a->status = -1; return; }
+    double mx = -INFINITY;
+    for (int sgm = 0; sgm < S; ++sgm) {
+      int lo = sgm * C, hi = (sgm + 1) * C;
+      if (hi > visible) hi = visible;
+      lse_part[sgm] = attend_range(pl, bt_row, h_kv, qd, a->scale, lo, hi, s_buf, opart);
+      for (int c = 0; c < D; ++c) o_part[(size_t)sgm * D + c] = opart[c];
+      if (lse_part[sgm] > mx) mx = lse_part[sgm];
+    }
+    for (int c = 0; c < D; ++c) out[c] = 0.0;
+    if (mx == -INFINITY) {
+      lse = -INFINITY;
+    } else {
+      double sum = 0.0;
+      for (int sgm = 0; sgm < S; ++sgm) sum += exp(lse_part[sgm] - mx);
+      lse = mx + log(sum);
+      for (int sgm = 0; sgm < S; ++sgm) {
+        if (lse_part[sgm] == -INFINITY) continue;
+        double w = exp(lse_part[sgm] - lse);
+        for (int c = 0; c < D; ++c) out[c] += w * o_part[(size_t)sgm * D + c];
+      }
+    }
+    free(lse_part);
+    free(o_part);
+  }
+  a->lse[(size_t)ri * a->Hq + hq] = lse;
+}
+
+static int check_pool(const orc_pool* pl, int Hq) {
+  if (!pl || !pl->k || !pl->v) return -1;
+  if (pl->num_kv_heads <= 0 || Hq <= 0 || Hq % pl->num_kv_heads) return -1;
+  if (pl->page_size <= 0 || pl->head_dim <= 0) return -1;
+  if (pl->dtype == ORC_INT8 && (!pl->k_scale || !pl->v_scale)) return -1;
+  return 0;
+}
+
+/*
+ * Attention of the listed query rows (all Hq heads each) over the paged
+ * cache.  q rows of sequence b are cu_q[b] .. cu_q[b+1]-1; seq_lens[b]
+ * counts every cached position of b, the rows' own included.  A decode step
+ * is the case cu_q = 0, 1, 2, ..., B.  Returns 0, or -1 on bad arguments.
+ */
+int orc_paged_attention(const orc_pool* pool, const uint16_t* q, const int32_t* cu_q, int B,
+                        int num_q_heads, const int32_t* block_table, int max_pages,
+                        const int32_t* seq_lens, double scale, const int32_t* rows,
+                        int nrows, int num_splits, double* out, double* lse, int nthreads) {
+  if (check_pool(pool, num_q_heads) || !q || !cu_q || !block_table || !seq_lens || !rows ||
+      !out || !lse || B <= 0 || nrows < 0)
+    return -1;
+  int maxL = 0;
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 0 || seq_lens[b] > max_pages * pool->page_size) return -1;
+    if (cu_q[b + 1] < cu_q[b]) return -1;   /* rows at negative positions see nothing */
+    if (seq_lens[b] > maxL) maxL = seq_lens[b];
+  }
+  attn_ctx ctx = {pool, q, cu_q, B, num_q_heads, block_table, max_pages, seq_lens, scale,
+                  rows, num_splits, out, lse, 0};
+  size_t scratch = (size_t)3 * pool->head_dim + (size_t)maxL + 1;
+  if (run_tasks(attn_task, &ctx, (long)nrows * num_q_heads, scratch, nthreads)) return -1;
+  return ctx.status;
+}
+
+/* ------------------------------------------------------------- KV writes */
+
+/*
+ * Position of new token i of sequence b: seq_lens[b] - n_b + i, with
+ * n_b = cu_new[b+1] - cu_new[b] (seq_lens already count the new tokens).
+ * Returns the flat slot index page * page_size + slot, or -1 if out of range.
+ */
+static long new_token_slot(const int32_t* block_table, int max_pages, int page_size,
+                           const int32_t* cu_new, const int32_t* seq_lens, int b, int i) {
+  int n = cu_new[b + 1] - cu_new[b];
+  int p = seq_lens[b] - n + i;
+  if (p < 0 || p >= max_pages * page_size) return -1;
+  int page = block_table[(size_t)b * max_pages + p / page_size];
+  return (long)page * page_size + p % page_size;
+}
+
+/* Copy the bf16 K/V vectors of the new tokens into their pool slots. */
+int orc_kv_append_bf16(uint16_t* pool_k, uint16_t* pool_v, int num_pages, int Hkv, int page_size,
+                       int D, const uint16_t* k_new, const uint16_t* v_new,
+                       const int32_t* cu_new, int B, const int32_t* block_table, int max_pages,
+                       const int32_t* seq_lens) {
+  for (int b = 0; b < B; ++b) {
+    for (int i = 0; i < cu_new[b + 1] - cu_new[b]; ++i) {
+      long fs = new_token_slot(block_table, max_pages, page_size, cu_new, seq_lens, b, i);
+      if (fs < 0) return -1;
+      long page = fs / page_size, slot = fs % page_size;
+      if (page >= num_pages) return -1;
+      int t = cu_new[b] + i;
+      for (int h = 0; h < Hkv; ++h) {
+        size_t dst = ((size_t)(page * Hkv + h) * page_size + slot) * D;
+        size_t src = ((size_t)t * Hkv + h) * D;
+        memcpy(pool_k + dst, k_new + src, sizeof(uint16_t) * (size_t)D);
+        memcpy(pool_v + dst, v_new + src, sizeof(uint16_t) * (size_t)D);
+      }
+    }
+  }
+  return 0;
+}
+
+/*
+ * One vector to int8 codes and an fp32 scale, every step in fp32:
+ * x_c = float(k_c), divided by w_c when a smoothing weight is given;
+ * amax = max_c |x_c|; scale = amax / 127; code_c = nearest-even integer to
+ * the fp32 quotient x_c / scale, clamped to [-127, 127].  amax = 0 gives
+ * scale 0 and all codes 0.
+ */
+void orc_quantize_row_int8(const uint16_t* x_bf16, const float* w, int D, int8_t* codes,
+                           float* scale_out) {
+  float amax = 0.0f;
+  for (int c = 0; c < D; ++c) {
+    float x = bf16_bits_to_float(x_bf16[c]);
+    if (w) x = x / w[c];
+    float ax = fabsf(x);
+    if (ax > amax) amax = ax;
+  }
+  float scale = amax / 127.0f;
+  *scale_out = scale;
+  for (int c = 0; c < D; ++c) {
+    if (scale == 0.0f) { codes[c] = 0; continue; }
+    float x = bf16_bits_to_float(x_bf16[c]);
+    if (w) x = x / w[c];
+    float qf = x / scale;
+    float r = nearbyintf(qf);   /* default rounding mode: to nearest, ties to even */
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    codes[c] = (int8_t)r;
+  }
+}
+
+/* Quantise the new K/V vectors (K smoothed by w if given) into the int8 pool. */
+int orc_kv_append_int8(int8_t* pool_k, int8_t* pool_v, float* k_scale, float* v_scale,
+                       int num_pages, int Hkv, int page_size, int D, const uint16_t* k_new,
+                       const uint16_t* v_new, const float* k_smooth, const int32_t* cu_new,
+                       int B, const int32_t* block_table, int max_pages,
+                       const int32_t* seq_lens) {
+  for (int b = 0; b < B; ++b) {
+    for (int i = 0; i < cu_new[b + 1] - cu_new[b]; ++i) {
+      long fs = new_token_slot(block_table, max_pages, page_size, cu_new, seq_lens, b, i);
+      if (fs < 0) return -1;
+      long page = fs / page_size, slot = fs % page_size;
+      if (page >= num_pages) return -1;
+      int t = cu_new[b] + i;
+      for (int h = 0; h < Hkv; ++h) {
+        size_t row = (size_t)(page * Hkv + h) * page_size + slot;
+        size_t src = ((size_t)t * Hkv + h) * D;
+        orc_quantize_row_int8(k_new + src, k_smooth, D, pool_k + row * D, &k_scale[row]);
+        orc_quantize_row_int8(v_new + src, NULL, D, pool_v + row * D, &v_scale[row]);
+      }
+    }
+  }
+  return 0;
+}

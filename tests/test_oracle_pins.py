@@ -1,0 +1,394 @@
+"""Pins for the fp64 oracle, independent of the oracle's own code.
+
+Each test checks the oracle against something the pages or the mathematics
+fix -- closed forms, invariants, a library routine on special cases, brute
+force on tiny inputs, hand-worked values -- chosen so that a dropped term, a
+wrong index or sign, or a transposed operand fails at least one of them.
+
+The method (TileInfer.jl "Performance" page, section "Fused kernels,
+FlashAttention and PagedAttention"): softmax attention over pages read in
+place through a block table; split-KV decode plus a combine; GQA heads.
+INT8 cache: one scale per cached vector ("INT8 KV cache" section).
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_flash_gb300 import workloads as W
+
+D = W.HEAD_DIM
+P = W.PAGE
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def make_pool_from_dense(rng, dense_k, dense_v, extra_pages=3):
+    """Scatter dense per-sequence K/V ([L_b][Hkv][D] uint16 bits) into a pool
+    through a random block table -- the inverse of the oracle's gather.
+    Unused pages and slots hold NaN, so a wrong gather shows."""
+    B = len(dense_k)
+    Hkv = dense_k[0].shape[1]
+    lens = np.array([k.shape[0] for k in dense_k], np.int32)
+    npg = (lens + P - 1) // P
+    num_pages = int(npg.sum()) + extra_pages
+    perm = rng.permutation(num_pages)
+    maxp = max(int(npg.max()), 1)
+    bt = np.full((B, maxp), num_pages - 1, np.int32)
+    kp = np.full((num_pages, Hkv, P, D), W.BF16_NAN, np.uint16)
+    vp = kp.copy()
+    off = 0
+    for b in range(B):
+        for j in range(npg[b]):
+            bt[b, j] = perm[off]
+            off += 1
+        for p in range(lens[b]):
+            kp[bt[b, p // P], :, p % P, :] = dense_k[b][p]
+            vp[bt[b, p // P], :, p % P, :] = dense_v[b][p]
+    return kp, vp, bt, lens
+
+
+def f(bits):
+    return W.bits_to_float(bits).astype(np.float64)
+
+
+def decode_cu(B):
+    return np.arange(B + 1, dtype=np.int32)
+
+
+# ------------------------------------------------------------ closed forms
+
+def test_single_key_returns_its_value_row():
+    rng = np.random.default_rng(1)
+    k = W.normal_bf16(rng, (1, 2, D))
+    v = W.normal_bf16(rng, (1, 2, D))
+    q = W.normal_bf16(rng, (1, 4, D))
+    kp, vp, bt, lens = make_pool_from_dense(rng, [k], [v])
+    s = 0.0883883
+    out, lse = oracle.paged_attention(kp, vp, q, decode_cu(1), bt, lens, s)
+    for h in range(4):
+        hk = h // 2
+        assert np.array_equal(out[0, h], f(v[0, hk]))           # exactly V
+        dot = math.fsum(f(q[0, h]) * f(k[0, hk]))
+        assert abs(lse[0, h] - s * dot) <= 1e-12 * max(1.0, abs(s * dot))
+
+
+def test_identical_keys_give_mean_of_values():
+    rng = np.random.default_rng(2)
+    L = 37                                              # 3 pages, ragged tail
+    k1 = W.normal_bf16(rng, (1, 1, D))
+    k = np.repeat(k1, L, axis=0)
+    v = W.normal_bf16(rng, (L, 1, D))
+    q = W.normal_bf16(rng, (1, 3, D))
+    kp, vp, bt, lens = make_pool_from_dense(rng, [k], [v])
+    s = 1 / math.sqrt(D)
+    out, lse = oracle.paged_attention(kp, vp, q, decode_cu(1), bt, lens, s)
+    mean = f(v[:, 0]).mean(axis=0)
+    for h in range(3):
+        np.testing.assert_allclose(out[0, h], mean, rtol=0, atol=1e-13)
+        dot = math.fsum(f(q[0, h]) * f(k1[0, 0]))
+        assert abs(lse[0, h] - (s * dot + math.log(L))) < 1e-12
+
+
+def test_zero_query_gives_uniform_weights():
+    rng = np.random.default_rng(3)
+    L = 50
+    k = W.normal_bf16(rng, (L, 2, D))
+    v = W.normal_bf16(rng, (L, 2, D))
+    q = np.zeros((1, 2, D), np.uint16)                 # bf16 +0
+    kp, vp, bt, lens = make_pool_from_dense(rng, [k], [v])
+    out, lse = oracle.paged_attention(kp, vp, q, decode_cu(1), bt, lens, 0.125)
+    for h in range(2):
+        np.testing.assert_allclose(out[0, h], f(v[:, h]).mean(axis=0), rtol=0, atol=1e-13)
+        assert abs(lse[0, h] - math.log(L)) < 1e-13
+
+
+def test_two_keys_logistic_weight():
+    rng = np.random.default_rng(4)
+    k = W.normal_bf16(rng, (2, 1, D))
+    v = W.normal_bf16(rng, (2, 1, D))
+    q = W.normal_bf16(rng, (1, 1, D))
+    kp, vp, bt, lens = make_pool_from_dense(rng, [k], [v])
+    s = 0.3
+    out, lse = oracle.paged_attention(kp, vp, q, decode_cu(1), bt, lens, s)
+    s1 = s * math.fsum(f(q[0, 0]) * f(k[0, 0]))
+    s2 = s * math.fsum(f(q[0, 0]) * f(k[1, 0]))
+    w1 = 1.0 / (1.0 + math.exp(s2 - s1))
+    np.testing.assert_allclose(out[0, 0], w1 * f(v[0, 0]) + (1 - w1) * f(v[1, 0]),
+                               rtol=0, atol=1e-13)
+    # lse of two terms: max + log1p(exp(-|s1 - s2|))
+    assert abs(lse[0, 0] - (max(s1, s2) + math.log1p(math.exp(-abs(s1 - s2))))) < 1e-13
+
+
+def test_gqa_grouping_is_consecutive():
+    """V constant per KV head: query head h must return the constant of KV head h // G."""
+    rng = np.random.default_rng(5)
+    Hkv, G, L = 4, 3, 20
+    consts = [1.0, -2.0, 0.5, 4.0]
+    k = W.normal_bf16(rng, (L, Hkv, D))
+    v = np.zeros((L, Hkv, D), np.uint16)
+    for h in range(Hkv):
+        v[:, h, :] = W.to_bf16_bits(np.full(D, consts[h], np.float32))
+    q = W.normal_bf16(rng, (1, Hkv * G, D))
+    kp, vp, bt, lens = make_pool_from_dense(rng, [k], [v])
+    out, _ = oracle.paged_attention(kp, vp, q, decode_cu(1), bt, lens, 0.1)
+    for hq in range(Hkv * G):
+        np.testing.assert_allclose(out[0, hq], consts[hq // G], rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------------------- invariants
+
+def test_page_permutation_leaves_output_bit_identical():
+    rng = np.random.default_rng(6)
+    case = W.decode_bf16(rng, [40, 71, 16, 1], Hq=4, Hkv=2)
+    cu = decode_cu(case.B)
+    out1, lse1 = oracle.paged_attention(case.k_pool, case.v_pool, case.q, cu,
+                                        case.layout.block_table, case.seq_lens, case.scale)
+    perm = rng.permutation(case.k_pool.shape[0])       # physical page p moves to perm[p]
+    kp2 = np.empty_like(case.k_pool)
+    vp2 = np.empty_like(case.v_pool)
+    kp2[perm] = case.k_pool
+    vp2[perm] = case.v_pool
+    bt2 = perm[case.layout.block_table].astype(np.int32)
+    out2, lse2 = oracle.paged_attention(kp2, vp2, case.q, cu, bt2, case.seq_lens, case.scale)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, "pages"])
+def test_split_plus_combine_equals_unsplit(S):
+    rng = np.random.default_rng(7)
+    case = W.decode_bf16(rng, [200, 33, 16, 97], Hq=8, Hkv=2)
+    cu = decode_cu(case.B)
+    args = (case.k_pool, case.v_pool, case.q, cu, case.layout.block_table, case.seq_lens,
+            case.scale)
+    ref, lref = oracle.paged_attention(*args)
+    nsplit = int((case.seq_lens.max() + P - 1) // P) if S == "pages" else S
+    out, lse = oracle.paged_attention(*args, num_splits=nsplit)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lref, rtol=0, atol=1e-12)
+
+
+def test_keys_after_the_causal_edge_do_not_matter():
+    rng = np.random.default_rng(8)
+    L, qlen = 45, 12
+    k = W.normal_bf16(rng, (L, 2, D))
+    v = W.normal_bf16(rng, (L, 2, D))
+    q = W.normal_bf16(rng, (qlen, 4, D))
+    kp, vp, bt, lens = make_pool_from_dense(rng, [k], [v])
+    cu = np.array([0, qlen], np.int32)
+    out1, lse1 = oracle.paged_attention(kp, vp, q, cu, bt, lens, 0.09)
+    # change K/V at positions > pos(row 5) = L - qlen + 5
+    edge = L - qlen + 5
+    k2, v2 = k.copy(), v.copy()
+    k2[edge + 1:] = W.normal_bf16(rng, k2[edge + 1:].shape)
+    v2[edge + 1:] = W.normal_bf16(rng, v2[edge + 1:].shape)
+    kp2, vp2 = kp.copy(), vp.copy()
+    for p in range(L):
+        kp2[bt[0, p // P], :, p % P] = k2[p]
+        vp2[bt[0, p // P], :, p % P] = v2[p]
+    out2, lse2 = oracle.paged_attention(kp2, vp2, q, cu, bt, lens, 0.09)
+    assert np.array_equal(out1[:6], out2[:6]) and np.array_equal(lse1[:6], lse2[:6])
+    assert not np.array_equal(out1[6:], out2[6:])
+
+
+# ------------------------------------------------ library routine: SDPA
+
+def _sdpa_reference(q, k, v, scale, qlen, L, G):
+    """torch's scaled_dot_product_attention in float64 with a bottom-right
+    causal mask, GQA by repeating KV heads; lse via torch.logsumexp."""
+    qt = torch.from_numpy(f(q)).permute(1, 0, 2)                  # [Hq][qlen][D]
+    kt = torch.from_numpy(f(k)).permute(1, 0, 2).repeat_interleave(G, dim=0)
+    vt = torch.from_numpy(f(v)).permute(1, 0, 2).repeat_interleave(G, dim=0)
+    i = torch.arange(qlen)[:, None]
+    j = torch.arange(L)[None, :]
+    mask = j <= (L - qlen + i)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask,
+                                                         scale=scale)
+    scores = (qt @ kt.transpose(1, 2)) * scale
+    lse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=-1)
+    return o.permute(1, 0, 2).numpy(), lse.permute(1, 0).numpy()
+
+
+@pytest.mark.parametrize("shape", [[(5, 37), (40, 40), (1, 1), (17, 33)],
+                                   [(16, 16), (3, 70)]])
+def test_causal_prefill_matches_sdpa(shape):
+    rng = np.random.default_rng(9)
+    Hkv, G = 2, 3
+    ks, vs, qs = [], [], []
+    for qlen, L in shape:
+        ks.append(W.normal_bf16(rng, (L, Hkv, D)))
+        vs.append(W.normal_bf16(rng, (L, Hkv, D)))
+        qs.append(W.normal_bf16(rng, (qlen, Hkv * G, D)))
+    kp, vp, bt, lens = make_pool_from_dense(rng, ks, vs)
+    cu = W.cu_from_counts([s[0] for s in shape])
+    scale = 1 / math.sqrt(D)
+    out, lse = oracle.paged_attention(kp, vp, np.concatenate(qs), cu, bt, lens, scale)
+    for b, (qlen, L) in enumerate(shape):
+        ro, rl = _sdpa_reference(qs[b], ks[b], vs[b], scale, qlen, L, G)
+        np.testing.assert_allclose(out[cu[b]:cu[b + 1]], ro, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[cu[b]:cu[b + 1]], rl, rtol=0, atol=1e-12)
+
+
+def test_row_subset_matches_full_evaluation():
+    rng = np.random.default_rng(10)
+    case = W.decode_bf16(rng, [30, 64, 5], Hq=4, Hkv=4)
+    cu = decode_cu(case.B)
+    args = (case.k_pool, case.v_pool, case.q, cu, case.layout.block_table, case.seq_lens,
+            case.scale)
+    full, lfull = oracle.paged_attention(*args)
+    sub, lsub = oracle.paged_attention(*args, rows=[2, 0])
+    assert np.array_equal(sub, full[[2, 0]]) and np.array_equal(lsub, lfull[[2, 0]])
+
+
+def test_empty_context_gives_zero_and_minus_inf():
+    rng = np.random.default_rng(11)
+    case = W.decode_bf16(rng, [0, 9], Hq=2, Hkv=1)
+    out, lse = oracle.paged_attention(case.k_pool, case.v_pool, case.q, decode_cu(2),
+                                      case.layout.block_table, case.seq_lens, case.scale)
+    assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(out[1]))
+
+
+# ----------------------------------------------------------------- INT8
+
+def _golden_cases():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "int8_half_even.txt")) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("case "):
+                cur = {"name": line[5:]}
+                cases.append(cur)
+            else:
+                key, vals = line.split(":", 1)
+                cur[key] = [float(x) for x in vals.split()]
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_int8_golden_vectors(case):
+    x = np.zeros(D, np.float32)
+    x[:len(case["x"])] = case["x"]
+    bits = W.to_bf16_bits(x)
+    assert np.array_equal(W.bits_to_float(bits), x)     # exactly representable
+    w = None
+    if "w" in case:
+        w = np.ones(D, np.float32)
+        w[:len(case["w"])] = case["w"]
+    codes, scale = oracle.quantize_row_int8(bits, w)
+    assert scale == np.float32(case["scale"][0])
+    exp = np.zeros(D, np.int8)
+    exp[:len(case["codes"])] = np.array(case["codes"], np.int8)
+    assert np.array_equal(codes, exp)
+
+
+def test_int8_random_vectors_match_numpy_float32_ieee():
+    """numpy's float32 division is IEEE round-to-nearest and np.rint rounds
+    half to even: the same fp32 steps, from an independent library."""
+    rng = np.random.default_rng(12)
+    for trial in range(200):
+        x = W.normal_bf16(rng, (D,))
+        w = W.smoothing_weight(rng) if trial % 2 else None
+        codes, scale = oracle.quantize_row_int8(x, w)
+        xf = W.bits_to_float(x)
+        if w is not None:
+            xf = (xf / w).astype(np.float32)
+        amax = np.float32(np.max(np.abs(xf)))
+        s = np.float32(amax / np.float32(127.0))
+        assert scale.view(np.uint32) == s.view(np.uint32)
+        ref = np.clip(np.rint((xf / s).astype(np.float32)), -127, 127).astype(np.int8)
+        assert np.array_equal(codes, ref)
+        assert np.abs(codes.astype(np.int32)).max() == 127       # amax maps to +-127
+
+
+def test_int8_requantising_dequantised_codes_is_idempotent():
+    rng = np.random.default_rng(13)
+    for _ in range(100):
+        x = W.normal_bf16(rng, (D,))
+        codes, scale = oracle.quantize_row_int8(x)
+        xd = (codes.astype(np.float32) * scale)
+        xb = W.to_bf16_bits(xd)
+        # dequantised values rounded back to bf16 keep their codes
+        codes2, _ = oracle.quantize_row_int8(xb)
+        assert np.array_equal(codes, codes2)
+
+
+def test_int8_cache_with_exact_codes_equals_bf16_cache():
+    """K/V chosen so that quantisation is exact (integer entries, max|x| = 127,
+    power-of-two smoothing weights): the INT8 attention must equal the bf16
+    attention bit for bit, which pins the dequantisation (code * scale * w)."""
+    rng = np.random.default_rng(14)
+    Hkv, G, L = 2, 2, 35
+    w = rng.choice([0.5, 1.0, 2.0], D).astype(np.float32)
+    xk = rng.integers(-127, 128, (L, Hkv, D)).astype(np.float32)
+    xk[:, :, 0] = 127.0
+    xv = rng.integers(-127, 128, (L, Hkv, D)).astype(np.float32)
+    xv[:, :, 1] = -127.0
+    kb = W.to_bf16_bits(xk * w)            # k = x * w, so k / w = x exactly
+    vb = W.to_bf16_bits(xv)
+    q = W.normal_bf16(rng, (1, Hkv * G, D))
+    kp, vp, bt, lens = make_pool_from_dense(rng, [kb], [vb])
+    cu_new = np.array([0, L], np.int32)
+    k8, v8, ks, vs = W.empty_pool_int8(kp.shape[0], Hkv)
+    k8, v8, ks, vs = oracle.kv_append_int8(k8, v8, ks, vs, kb, vb, cu_new, bt, lens, k_smooth=w)
+    for p in range(L):
+        assert np.all(ks[bt[0, p // P], :, p % P] == 1.0)
+        assert np.all(vs[bt[0, p // P], :, p % P] == 1.0)
+    o_bf, l_bf = oracle.paged_attention(kp, vp, q, decode_cu(1), bt, lens, 0.1)
+    o_i8, l_i8 = oracle.paged_attention(k8, v8, q, decode_cu(1), bt, lens, 0.1,
+                                        k_scale=ks, v_scale=vs, k_smooth=w)
+    assert np.array_equal(o_bf, o_i8) and np.array_equal(l_bf, l_i8)
+
+
+# ----------------------------------------------------------------- appends
+
+def test_bf16_append_writes_exactly_the_named_slots():
+    rng = np.random.default_rng(15)
+    Hkv = 3
+    lens_before = np.array([0, 14, 31], np.int32)
+    n_new = np.array([20, 5, 1], np.int32)
+    lens = lens_before + n_new
+    layout = W.scatter_pages(rng, lens)
+    kp, vp = W.empty_pool_bf16(layout.num_pages, Hkv)
+    T = int(n_new.sum())
+    k_new = W.normal_bf16(rng, (T, Hkv, D))
+    v_new = W.normal_bf16(rng, (T, Hkv, D))
+    cu = W.cu_from_counts(n_new)
+    k2, v2 = oracle.kv_append_bf16(kp, vp, k_new, v_new, cu, layout.block_table, lens)
+    touched = np.zeros(kp.shape[:3], bool)
+    for b in range(3):
+        for i in range(n_new[b]):
+            p = lens_before[b] + i
+            page = layout.block_table[b, p // P]
+            assert np.array_equal(k2[page, :, p % P], k_new[cu[b] + i])
+            assert np.array_equal(v2[page, :, p % P], v_new[cu[b] + i])
+            touched[page, :, p % P] = True
+    assert np.all(k2[~touched] == W.BF16_NAN) and np.all(v2[~touched] == W.BF16_NAN)
+
+
+def test_int8_append_rows_are_quantised_rows():
+    rng = np.random.default_rng(16)
+    Hkv = 2
+    lens = np.array([19], np.int32)
+    layout = W.scatter_pages(rng, lens)
+    w = W.smoothing_weight(rng)
+    k_new = W.keys_with_channel_weight(rng, (19, Hkv, D), w)
+    v_new = W.normal_bf16(rng, (19, Hkv, D))
+    k8, v8, ks, vs = W.empty_pool_int8(layout.num_pages, Hkv)
+    k8, v8, ks, vs = oracle.kv_append_int8(k8, v8, ks, vs, k_new, v_new,
+                                           W.cu_from_counts([19]), layout.block_table, lens,
+                                           k_smooth=w)
+    touched = np.zeros(k8.shape[:3], bool)
+    for p in range(19):
+        page = layout.block_table[0, p // P]
+        for h in range(Hkv):
+            ck, sk = oracle.quantize_row_int8(k_new[p, h], w)
+            cv, sv = oracle.quantize_row_int8(v_new[p, h])
+            assert np.array_equal(k8[page, h, p % P], ck) and ks[page, h, p % P] == sk
+            assert np.array_equal(v8[page, h, p % P], cv) and vs[page, h, p % P] == sv
+            touched[page, h, p % P] = True
+    assert np.all(np.isnan(ks[~touched])) and np.all(k8[~touched] == 0x5A)
