@@ -1,0 +1,183 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: attention over a paged KV cache on one
+ * GB300 (sm_103a).
+ *
+ * The operations follow the TileInfer.jl "Performance" page:
+ *  - section "Fused kernels, FlashAttention and PagedAttention": the KV cache
+ *    write, paged flash attention as an online softmax over the pages read in
+ *    place through the block table, split-KV for decode, and a combine kernel
+ *    kept separate from the split kernel;
+ *  - section "INT8 KV cache": an INT8 cache with one scale per cached vector,
+ *    keys smoothed by the key norm's weight;
+ *  - section "Speculative decoding", "Attention for verify steps": the prefill
+ *    kernel runs a block per head over every page.
+ *
+ * Conventions (all calls):
+ *  - Every pointer argument is a DEVICE pointer unless its comment says host.
+ *    The caller owns all memory; the library allocates nothing on any call.
+ *  - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *    void*; NULL means the legacy default stream).  A status other than
+ *    PKV_OK means nothing was launched, except PKV_ERR_CUDA, which reports a
+ *    failed launch.
+ *  - Arguments are checked on the host before any launch: a NULL pointer
+ *    that is required, head_dim != 128, page_size != 16, num_q_heads not a
+ *    multiple of num_kv_heads, negative sizes or a short workspace return
+ *    PKV_ERR_INVALID.  The CONTENTS of device arrays (block tables, sequence
+ *    lengths, offsets) are the caller's contract and are not read on the host.
+ *  - bf16 tensors hold IEEE bfloat16; fp32 is IEEE binary32.
+ *  - GQA: query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *  - lse is the natural-log log-sum-exp of the scaled scores, softmax_scale *
+ *    q.k, over the keys a row sees; a row that sees no key gets out = 0 and
+ *    lse = -inf.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID = -1,      /* bad argument; nothing launched */
+  PKV_ERR_UNSUPPORTED = -2,  /* valid but not provided (e.g. INT8 prefill) */
+  PKV_ERR_CUDA = -3,         /* a CUDA call or launch failed */
+  PKV_ERR_TIMEOUT = -4       /* a kernel's bounded wait ran out (pkv_poll_device_error) */
+} pkv_status;
+
+typedef enum { PKV_BF16 = 0, PKV_INT8 = 1 } pkv_kv_dtype;
+
+/*
+ * One paged KV pool (TileInfer.jl "Performance" page: "the pool", read
+ * "through the block table").  K and V are separate arrays of
+ * [num_pages][num_kv_heads][page_size][head_dim]; one (page, head) slab is
+ * contiguous (4 KiB for bf16, 2 KiB for int8).  For PKV_INT8, k_scale and
+ * v_scale hold one fp32 scale per cached vector, [num_pages][num_kv_heads]
+ * [page_size] ("INT8 KV cache": one scale per cached vector); for PKV_BF16
+ * they must be NULL.  k and v must be 16-byte aligned.  Position p of
+ * sequence b lives in page block_table[b][p / page_size], slot p % page_size.
+ */
+typedef struct {
+  void* k;
+  void* v;
+  float* k_scale;
+  float* v_scale;
+  int32_t num_pages;
+  int32_t num_kv_heads;
+  int32_t page_size;   /* must be 16 */
+  int32_t head_dim;    /* must be 128 */
+  int32_t dtype;       /* pkv_kv_dtype */
+} pkv_pool;
+
+/*
+ * kv_append -- write new K/V vectors into the pool pages named by the block
+ * table ("Fused kernels ...": the KV cache write; "INT8 KV cache": one scale
+ * per vector).
+ *
+ *  k_new, v_new  bf16 [num_tokens][num_kv_heads][128]; rows cu_new[b] ..
+ *                cu_new[b+1]-1 belong to sequence b.
+ *  cu_new        int32 [batch+1], non-decreasing, cu_new[batch] = num_tokens.
+ *  block_table   int32 [batch][max_pages] page ids.
+ *  seq_lens      int32 [batch] cached positions of each sequence AFTER this
+ *                append; new row i of sequence b goes to position
+ *                seq_lens[b] - n_b + i, n_b = cu_new[b+1] - cu_new[b].
+ *  k_smooth      fp32 [128] per-channel key weight (> 0) or NULL.  INT8
+ *                pools only: keys are divided by it before quantisation.
+ *                Must be NULL for bf16 pools.
+ *
+ * bf16 pools: the vectors are copied bit for bit.  INT8 pools: per vector x
+ * (fp32; k / w for smoothed keys), scale = max|x| / 127 in fp32, code =
+ * round-half-even(x / scale) as an IEEE fp32 quotient, clamped to +-127; an
+ * all-zero vector stores scale 0 and codes 0.  Slots not named are left
+ * untouched.  num_tokens == 0 launches nothing and returns PKV_OK.
+ */
+pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
+                         int32_t num_tokens, const int32_t* cu_new, int32_t batch,
+                         const int32_t* block_table, int32_t max_pages,
+                         const int32_t* seq_lens, const float* k_smooth, void* stream);
+
+/*
+ * Split plan of a decode call ("Fused kernels ...": split-KV for decode).
+ * Host-only; launches nothing.  max_seq_len (host) bounds every seq_lens[b];
+ * num_splits 0 asks for the built-in heuristic (split count chosen from the
+ * batch, the heads and the device's SM count), > 0 forces that many splits.
+ * Outputs (host pointers, each may be NULL): the split count S, the pages per
+ * split, and the workspace bytes the decode call needs (0 when S == 1).
+ */
+pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t max_seq_len, int32_t num_splits, int32_t* splits_out,
+                           int32_t* pages_per_split_out, size_t* workspace_bytes_out);
+
+/*
+ * paged_attn_decode -- one query token per sequence against its cached
+ * positions 0 .. seq_lens[b]-1 (the token's own position included): split-KV
+ * partials, then a log-sum-exp combine ("Fused kernels ...": online softmax
+ * over the pages in place, split-KV for decode, separate combine kernel).
+ *
+ *  q            bf16 [batch][num_q_heads][128].
+ *  block_table  int32 [batch][max_pages]; seq_lens int32 [batch] (device);
+ *               max_seq_len (host) >= every seq_lens[b].
+ *  k_smooth     INT8 pools: the same fp32 [128] weight given to kv_append,
+ *               or NULL if the keys were not smoothed; NULL for bf16.
+ *  num_splits   0 = heuristic, > 0 forces (see pkv_decode_plan).
+ *  workspace    fp32 scratch of at least pkv_decode_plan's bytes (256-byte
+ *               aligned), may be NULL when that is 0.  Holds the split
+ *               partials; its contents are dead after the call.
+ *  out          bf16 [batch][num_q_heads][128]; lse fp32 [batch][num_q_heads]
+ *               or NULL.
+ */
+pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t batch,
+                                 int32_t num_q_heads, const int32_t* block_table,
+                                 int32_t max_pages, const int32_t* seq_lens,
+                                 int32_t max_seq_len, float softmax_scale,
+                                 const float* k_smooth, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, void* out, float* lse, void* stream);
+
+/*
+ * paged_attn_prefill -- causal attention of a chunk of new query rows per
+ * sequence against the sequence's cached prefix plus the chunk itself
+ * (a block of query rows per head over every page: "Attention for verify
+ * steps"; chunked prefill: "What is left to gain").  Tensor-core (tcgen05)
+ * QK^T and PV with fp32 accumulation; P is rounded to bf16 for PV.
+ *
+ *  q         bf16 [total_q][num_q_heads][128]; rows cu_q[b] .. cu_q[b+1]-1
+ *            belong to sequence b.  cu_q int32 [batch+1] (device).
+ *  seq_lens  int32 [batch] cached positions INCLUDING this chunk (append the
+ *            chunk's K/V first).  Row i of sequence b sits at position
+ *            seq_lens[b] - q_b + i and sees keys 0 .. that position
+ *            (bottom-right causal alignment).
+ *  max_q_len (host) >= every q_b.
+ *  out       bf16 [total_q][num_q_heads][128]; lse fp32 [total_q][num_q_heads]
+ *            or NULL.
+ * bf16 pools only (PKV_ERR_UNSUPPORTED for INT8).
+ */
+pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, const int32_t* cu_q,
+                                  int32_t batch, int32_t num_q_heads,
+                                  const int32_t* block_table, int32_t max_pages,
+                                  const int32_t* seq_lens, int32_t max_q_len,
+                                  float softmax_scale, void* out, float* lse, void* stream);
+
+/*
+ * Synchronises the stream, then reports and clears the device-side error
+ * words of the kernels: PKV_ERR_TIMEOUT if a bounded wait ran out (its
+ * outputs are garbage), else PKV_ERR_INVALID if a device-side check of the
+ * caller's arrays failed (a position past the block table, a page id outside
+ * the pool: the offending row was skipped), else PKV_OK.  PKV_ERR_CUDA if
+ * the stream itself reports an error.  Host-blocking.
+ */
+pkv_status pkv_poll_device_error(void* stream);
+
+/* Static text for a status code. */
+const char* pkv_status_string(pkv_status status);
+
+/* Number of SMs the split heuristic assumes for the current device (host). */
+int32_t pkv_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

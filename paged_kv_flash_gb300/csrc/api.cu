@@ -1,0 +1,227 @@
+// api.cu -- the extern "C" entry points of libpagedkv.so (declared in
+// include/pagedkv.h): host-side argument checks, the split-count heuristic
+// and kernel dispatch.  Nothing here allocates device or host memory.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace pkv_host {
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  static int cached_dev = -1, cached = 0;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    cached = n;
+    cached_dev = dev;
+  }
+  return cached;
+}
+
+}  // namespace pkv_host
+
+namespace {
+
+using pkv_host::sm_count;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+pkv_status check_pool(const pkv_pool* pool) {
+  if (!pool || !pool->k || !pool->v) return PKV_ERR_INVALID;
+  if (pool->head_dim != pkv::kHeadDim || pool->page_size != pkv::kPageSize)
+    return PKV_ERR_INVALID;
+  if (pool->num_pages <= 0 || pool->num_kv_heads <= 0) return PKV_ERR_INVALID;
+  if (!aligned(pool->k, 16) || !aligned(pool->v, 16)) return PKV_ERR_INVALID;
+  if (pool->dtype == PKV_BF16) {
+    if (pool->k_scale || pool->v_scale) return PKV_ERR_INVALID;
+  } else if (pool->dtype == PKV_INT8) {
+    if (!pool->k_scale || !pool->v_scale) return PKV_ERR_INVALID;
+    if (!aligned(pool->k_scale, 16) || !aligned(pool->v_scale, 16)) return PKV_ERR_INVALID;
+  } else {
+    return PKV_ERR_INVALID;
+  }
+  return PKV_OK;
+}
+
+// Split plan: pages per split C and split count S for a decode call.
+//
+// The split kernel runs one CTA per (split, KV head, sequence) with 4 warps,
+// two CTAs resident per SM.  The heuristic aims for about eight waves of
+// CTAs, estimated from the longest sequence, so that sequences of unequal
+// length balance across the SMs; a split covers 4 to 32 pages (64 to 512
+// positions) and C is a multiple of the 4 warps so that they get equal work.
+// A forced split count S gives C = ceil(pages / S).
+struct Plan {
+  int splits, pages_per_split;
+  size_t ws_bytes, ws_lse_offset;
+};
+
+Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, int num_splits) {
+  const int mp = std::max(1, (max_seq_len + pkv::kPageSize - 1) / pkv::kPageSize);
+  int C;
+  if (num_splits > 0) {
+    C = (mp + num_splits - 1) / num_splits;
+  } else {
+    const long long slots = (long long)sm_count() * pkv_host::kDecodeCtasPerSm;
+    const long long page_heads = (long long)batch * num_kv_heads * mp;
+    long long c = (page_heads + 8 * slots - 1) / (8 * slots);
+    c = std::max<long long>(4, std::min<long long>(32, c));
+    c = (c + pkv_host::kDecodeWarps - 1) / pkv_host::kDecodeWarps * pkv_host::kDecodeWarps;
+    C = (int)std::min<long long>(c, mp);
+  }
+  C = std::max(1, C);
+  Plan p;
+  p.splits = (mp + C - 1) / C;
+  p.pages_per_split = C;
+  if (p.splits == 1) {
+    p.ws_bytes = 0;
+    p.ws_lse_offset = 0;
+  } else {
+    const size_t rows = (size_t)batch * num_q_heads * p.splits;
+    const size_t o_bytes = rows * pkv::kHeadDim * sizeof(float);
+    p.ws_lse_offset = (o_bytes + 255) / 256 * 256;
+    p.ws_bytes = p.ws_lse_offset + (rows * sizeof(float) + 255) / 256 * 256;
+  }
+  return p;
+}
+
+pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_new,
+                         int32_t num_tokens, const int32_t* cu_new, int32_t batch,
+                         const int32_t* block_table, int32_t max_pages,
+                         const int32_t* seq_lens, const float* k_smooth, void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0 || batch < 0 || max_pages < 0) return PKV_ERR_INVALID;
+  if (num_tokens == 0) return PKV_OK;
+  if (batch == 0 || max_pages == 0) return PKV_ERR_INVALID;
+  if (!k_new || !v_new || !cu_new || !block_table || !seq_lens) return PKV_ERR_INVALID;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PKV_ERR_INVALID;
+  if (pool->dtype == PKV_BF16 && k_smooth) return PKV_ERR_INVALID;
+  if (k_smooth && !aligned(k_smooth, 16)) return PKV_ERR_INVALID;
+  pkv_host::AppendLaunch a{pool->k, pool->v, pool->k_scale, pool->v_scale, pool->num_pages,
+                           pool->num_kv_heads, k_new, v_new, num_tokens, cu_new, batch,
+                           block_table, max_pages, seq_lens, k_smooth};
+  return cuda_status(pkv_host::launch_append(a, pool->dtype == PKV_INT8,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t max_seq_len, int32_t num_splits, int32_t* splits_out,
+                           int32_t* pages_per_split_out, size_t* workspace_bytes_out) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+      max_seq_len < 0 || num_splits < 0)
+    return PKV_ERR_INVALID;
+  const Plan p = make_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits);
+  if (splits_out) *splits_out = p.splits;
+  if (pages_per_split_out) *pages_per_split_out = p.pages_per_split;
+  if (workspace_bytes_out) *workspace_bytes_out = p.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t batch,
+                                 int32_t num_q_heads, const int32_t* block_table,
+                                 int32_t max_pages, const int32_t* seq_lens,
+                                 int32_t max_seq_len, float softmax_scale,
+                                 const float* k_smooth, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, void* out, float* lse, void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads || max_pages <= 0 ||
+      max_seq_len < 0 || (long long)max_seq_len > (long long)max_pages * pkv::kPageSize ||
+      num_splits < 0 || !std::isfinite(softmax_scale))
+    return PKV_ERR_INVALID;
+  if (!pkv_host::decode_supports_group(num_q_heads / pool->num_kv_heads))
+    return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!q || !block_table || !seq_lens || !out) return PKV_ERR_INVALID;
+  if (pool->dtype == PKV_BF16 && k_smooth) return PKV_ERR_INVALID;
+  const Plan p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, num_splits);
+  if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned(workspace, 256)))
+    return PKV_ERR_INVALID;
+  if ((long long)batch > 65535 || p.splits > 2147483647 / 2) return PKV_ERR_UNSUPPORTED;
+  pkv_host::DecodeLaunch a{};
+  a.k = pool->k;
+  a.v = pool->v;
+  a.k_scale = pool->k_scale;
+  a.v_scale = pool->v_scale;
+  a.num_pages = pool->num_pages;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.q = q;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.softmax_scale = softmax_scale;
+  a.k_smooth = k_smooth;
+  a.splits = p.splits;
+  a.pages_per_split = p.pages_per_split;
+  a.ws_o = p.ws_bytes ? static_cast<float*>(workspace) : nullptr;
+  a.ws_lse = p.ws_bytes
+                 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ws_lse_offset)
+                 : nullptr;
+  a.out = out;
+  a.lse = lse;
+  return cuda_status(pkv_host::launch_decode(a, pool->dtype == PKV_INT8,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, const int32_t* cu_q,
+                                  int32_t batch, int32_t num_q_heads,
+                                  const int32_t* block_table, int32_t max_pages,
+                                  const int32_t* seq_lens, int32_t max_q_len,
+                                  float softmax_scale, void* out, float* lse, void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads || max_pages <= 0 ||
+      max_q_len < 0 || !std::isfinite(softmax_scale))
+    return PKV_ERR_INVALID;
+  if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0 || max_q_len == 0) return PKV_OK;
+  if (!q || !cu_q || !block_table || !seq_lens || !out) return PKV_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(out, 16)) return PKV_ERR_INVALID;
+  if (batch > 65535 || num_q_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  pkv_host::PrefillLaunch a{pool->k, pool->v, pool->num_pages, pool->num_kv_heads, q, cu_q,
+                            batch, num_q_heads, block_table, max_pages, seq_lens, max_q_len,
+                            softmax_scale, out, lse};
+  cudaError_t e = pkv_host::launch_prefill(a, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+pkv_status pkv_poll_device_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
+  const uint32_t e = pkv_host::take_append_error(s) | pkv_host::take_decode_error(s) |
+                     pkv_host::take_prefill_error(s);
+  if (e == ~0u) return PKV_ERR_CUDA;
+  if (e & pkv::kErrTimeout) return PKV_ERR_TIMEOUT;
+  return e ? PKV_ERR_INVALID : PKV_OK;
+}
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_TIMEOUT: return "device-side wait timed out or device-side check failed";
+  }
+  return "unknown status";
+}
+
+int32_t pkv_device_sm_count(void) { return sm_count(); }
+
+}  // extern "C"

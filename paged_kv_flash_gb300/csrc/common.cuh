@@ -1,0 +1,173 @@
+// common.cuh -- device helpers shared by the sm_103a kernels of libpagedkv.
+//
+// Everything here is plain PTX for sm_103a: mbarriers with bounded waits,
+// bulk (TMA-engine) copies, bf16/int8 unpacking and packed f32x2 arithmetic.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+constexpr int kHeadDim = 128;
+constexpr int kPageSize = 16;
+
+// Bits of the device error word (one word per translation unit, read and
+// cleared by pkv_poll_device_error).
+constexpr uint32_t kErrTimeout = 1u;       // a bounded wait ran out
+constexpr uint32_t kErrBadIndex = 2u;      // a block-table / position check failed
+
+// Wall-clock limit of every spin-wait in these kernels (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ------------------------------------------------------------- mbarriers
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Gives up after
+// kWaitLimitNs of wall-clock time and returns false; never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// --------------------------------------------------------- bulk copies
+
+// One contiguous global -> shared copy by the TMA engine; completion is
+// signalled as transaction bytes on the mbarrier.  Addresses 16-byte aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Same, with an L2 eviction-priority hint (streamed data: evict first).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// ------------------------------------------------------------ unpacking
+
+// Two bf16 packed in a 32-bit word -> (low, high) as fp32 (exact).
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Signed byte i (0..3) of a word -> fp32, exactly: the byte (offset by 128)
+// becomes the low mantissa bits of 2^23, then the bias is subtracted.
+template <int I>
+__device__ __forceinline__ uint32_t i8_biased_bits(uint32_t w_xor80) {
+  return __byte_perm(w_xor80, 0x4B000000u, 0x7540u + I);
+}
+constexpr float kI8Bias = 8388736.0f;  // 2^23 + 128
+
+// ------------------------------------------------- packed f32x2 helpers
+
+union F2 {
+  float2 f;
+  unsigned long long u;
+};
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  F2 x, y, z, r;
+  x.f = a;
+  y.f = b;
+  z.f = c;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.u) : "l"(x.u), "l"(y.u), "l"(z.u));
+  return r.f;
+}
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  F2 x, y, r;
+  x.f = a;
+  y.f = b;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
+  return r.f;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  F2 x, y, r;
+  x.f = a;
+  y.f = b;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.u) : "l"(x.u), "l"(y.u));
+  return r.f;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+}  // namespace pkv
+
+// Host-side helpers shared by the translation units.
+namespace pkv_host {
+int sm_count();                 // cached SM count of the current device
+}

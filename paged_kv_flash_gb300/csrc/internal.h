@@ -1,0 +1,80 @@
+// internal.h -- host-side interface between the C ABI (api.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pkv_host {
+
+struct AppendLaunch {
+  void* k;                 // pool K (bf16 or int8)
+  void* v;
+  float* k_scale;          // int8 only
+  float* v_scale;
+  int num_pages, num_kv_heads;
+  const void* k_new;       // bf16 [T][Hkv][128]
+  const void* v_new;
+  int num_tokens;
+  const int32_t* cu_new;   // [B+1]
+  int batch;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  const float* k_smooth;   // int8 only, may be null
+};
+
+cudaError_t launch_append(const AppendLaunch& a, bool int8, cudaStream_t s);
+uint32_t take_append_error(cudaStream_t s);
+
+struct DecodeLaunch {
+  const void* k;
+  const void* v;
+  const float* k_scale;
+  const float* v_scale;
+  int num_pages, num_kv_heads;
+  const void* q;           // bf16 [B][Hq][128]
+  int batch, num_q_heads;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  float softmax_scale;
+  const float* k_smooth;
+  int splits, pages_per_split;
+  float* ws_o;             // [B][Hq][splits][128] when splits > 1
+  float* ws_lse;           // [B][Hq][splits]
+  void* out;               // bf16 [B][Hq][128]
+  float* lse;              // [B][Hq] or null
+};
+
+// Kernel geometry the split heuristic needs.
+constexpr int kDecodeWarps = 4;          // warps per split CTA
+constexpr int kDecodeCtasPerSm = 2;      // resident split CTAs per SM (by smem)
+
+bool decode_supports_group(int group);
+cudaError_t launch_decode(const DecodeLaunch& a, bool int8, cudaStream_t s);
+uint32_t take_decode_error(cudaStream_t s);
+
+struct PrefillLaunch {
+  const void* k;
+  const void* v;
+  int num_pages, num_kv_heads;
+  const void* q;           // bf16 [total_q][Hq][128]
+  const int32_t* cu_q;     // [B+1]
+  int batch, num_q_heads;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  int max_q_len;
+  float softmax_scale;
+  void* out;
+  float* lse;
+};
+
+cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s);
+uint32_t take_prefill_error(cudaStream_t s);
+
+int sm_count();
+
+}  // namespace pkv_host

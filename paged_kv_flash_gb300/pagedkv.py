@@ -1,0 +1,222 @@
+"""ctypes binding over libpagedkv.so (C ABI in include/pagedkv.h).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  Tensors are torch CUDA tensors (PyTorch supplies
+device memory and streams); the library itself allocates nothing, so where a
+call needs an output or a workspace and none is given, this binding
+allocates it with torch before the call.
+
+There is no fallback: if the library is missing or fails to load, importing
+this module raises.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4
+BF16, INT8 = 0, 1
+HEAD_DIM, PAGE_SIZE = 128, 16
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib.pkv_status_string(status).decode()} ({status})")
+
+
+class _Pool(ctypes.Structure):
+    _fields_ = [
+        ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32),
+    ]
+
+
+# Every symbol include/pagedkv.h declares, with its ctypes signature.
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+_POOLP = ctypes.POINTER(_Pool)
+SIGNATURES = {
+    "pkv_kv_append": (_I, [_POOLP, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P]),
+    "pkv_decode_plan": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                             ctypes.POINTER(_SZ)]),
+    "pkv_paged_attn_decode": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P, _SZ,
+                                   _P, _P, _P]),
+    "pkv_paged_attn_prefill": (_I, [_POOLP, _P, _P, _I, _I, _P, _I, _P, _I, _F, _P, _P, _P]),
+    "pkv_poll_device_error": (_I, [_P]),
+    "pkv_status_string": (ctypes.c_char_p, [_I]),
+    "pkv_device_sm_count": (_I, []),
+}
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"{_LIB_PATH} is not built; run paged_kv_flash_gb300.build.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise PkvError(status, what)
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got "
+                         f"{t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
+
+
+@dataclass
+class Pool:
+    """A paged KV pool: k, v [num_pages][Hkv][16][128] (bf16 or int8) and, for
+    int8, fp32 scales [num_pages][Hkv][16]."""
+    k: torch.Tensor
+    v: torch.Tensor
+    k_scale: Optional[torch.Tensor] = None
+    v_scale: Optional[torch.Tensor] = None
+
+    @property
+    def dtype(self) -> int:
+        return INT8 if self.k.dtype == torch.int8 else BF16
+
+    @property
+    def num_pages(self) -> int:
+        return self.k.shape[0]
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.k.shape[1]
+
+    def c(self) -> _Pool:
+        return _Pool(self.k.data_ptr(), self.v.data_ptr(),
+                     self.k_scale.data_ptr() if self.k_scale is not None else None,
+                     self.v_scale.data_ptr() if self.v_scale is not None else None,
+                     self.k.shape[0], self.k.shape[1], self.k.shape[2], self.k.shape[3],
+                     self.dtype)
+
+    @staticmethod
+    def empty(num_pages: int, num_kv_heads: int, dtype=torch.bfloat16, device="cuda"):
+        shape = (num_pages, num_kv_heads, PAGE_SIZE, HEAD_DIM)
+        if dtype == torch.int8:
+            return Pool(torch.empty(shape, dtype=torch.int8, device=device),
+                        torch.empty(shape, dtype=torch.int8, device=device),
+                        torch.empty(shape[:3], dtype=torch.float32, device=device),
+                        torch.empty(shape[:3], dtype=torch.float32, device=device))
+        return Pool(torch.empty(shape, dtype=torch.bfloat16, device=device),
+                    torch.empty(shape, dtype=torch.bfloat16, device=device))
+
+
+def kv_append(pool: Pool, k_new, v_new, cu_new, block_table, seq_lens, k_smooth=None,
+              stream=None):
+    """Write k_new/v_new [T][Hkv][128] bf16 into the pool (see pkv_kv_append)."""
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    for t, n in ((cu_new, "cu_new"), (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _need(t, torch.int32, n)
+    if k_smooth is not None:
+        _need(k_smooth, torch.float32, "k_smooth")
+    pc = pool.c()
+    st = _lib.pkv_kv_append(ctypes.byref(pc), _ptr(k_new), _ptr(v_new), k_new.shape[0],
+                            _ptr(cu_new), seq_lens.shape[0], _ptr(block_table),
+                            block_table.shape[1], _ptr(seq_lens), _ptr(k_smooth),
+                            _stream(stream))
+    _check(st, "pkv_kv_append")
+
+
+def decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits=0):
+    """(splits, pages_per_split, workspace_bytes) of a decode call."""
+    s, c, w = _I(), _I(), _SZ()
+    st = _lib.pkv_decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits,
+                              ctypes.byref(s), ctypes.byref(c), ctypes.byref(w))
+    _check(st, "pkv_decode_plan")
+    return s.value, c.value, w.value
+
+
+def paged_attn_decode(pool: Pool, q, block_table, seq_lens, max_seq_len, softmax_scale,
+                      k_smooth=None, num_splits=0, workspace=None, out=None, lse=None,
+                      want_lse=True, stream=None):
+    """One query token per sequence: q [B][Hq][128] bf16 -> (out bf16, lse fp32)."""
+    _need(q, torch.bfloat16, "q")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, _ = q.shape
+    _, _, ws_bytes = decode_plan(B, Hq, pool.num_kv_heads, max_seq_len, num_splits)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    pc = pool.c()
+    st = _lib.pkv_paged_attn_decode(
+        ctypes.byref(pc), _ptr(q), B, Hq, _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), int(max_seq_len), float(softmax_scale), _ptr(k_smooth),
+        int(num_splits), _ptr(workspace), workspace.numel() if workspace is not None else 0,
+        _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "pkv_paged_attn_decode")
+    return out, lse
+
+
+def paged_attn_prefill(pool: Pool, q, cu_q, block_table, seq_lens, max_q_len, softmax_scale,
+                       out=None, lse=None, want_lse=True, stream=None):
+    """Causal chunk attention: q [total_q][Hq][128] bf16 -> (out bf16, lse fp32)."""
+    _need(q, torch.bfloat16, "q")
+    for t, n in ((cu_q, "cu_q"), (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _need(t, torch.int32, n)
+    T, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    pc = pool.c()
+    st = _lib.pkv_paged_attn_prefill(
+        ctypes.byref(pc), _ptr(q), _ptr(cu_q), seq_lens.shape[0], Hq, _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), int(max_q_len), float(softmax_scale), _ptr(out),
+        _ptr(lse), _stream(stream))
+    _check(st, "pkv_paged_attn_prefill")
+    return out, lse
+
+
+def poll_device_error(stream=None) -> int:
+    """Synchronise and return the status of the kernels' device-side checks."""
+    return _lib.pkv_poll_device_error(_stream(stream))
+
+
+def sm_count() -> int:
+    return _lib.pkv_device_sm_count()
+
+
+def status_string(status: int) -> str:
+    return _lib.pkv_status_string(status).decode()
+
+
+def raw():
+    """The loaded ctypes library (for tests that exercise the C ABI directly)."""
+    return _lib

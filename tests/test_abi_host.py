@@ -1,0 +1,158 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+symbol include/pagedkv.h declares, and rejects bad arguments before any
+launch (no GPU needed: these paths never reach the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_flash_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    syms = declared_symbols()
+    for name in ("pkv_kv_append", "pkv_paged_attn_decode", "pkv_paged_attn_prefill"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_binding_covers_every_declared_symbol():
+    import importlib.util
+    spec = importlib.util.find_spec("paged_kv_flash_gb300.pagedkv")
+    src = open(spec.origin).read()
+    for name in declared_symbols():
+        assert f'"{name}"' in src, f"{name} has no binding signature"
+
+
+class Pool(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+FAKE = 1 << 20          # a non-null, 256-aligned address that is never dereferenced
+
+
+def good_pool(**kw):
+    p = dict(k=FAKE, v=FAKE * 2, k_scale=None, v_scale=None, num_pages=4, num_kv_heads=2,
+             page_size=16, head_dim=128, dtype=0)
+    p.update(kw)
+    return Pool(**p)
+
+
+def decode(lib, pool, **kw):
+    a = dict(q=FAKE, B=1, Hq=4, bt=FAKE, max_pages=4, sl=FAKE, max_seq_len=64, scale=0.1,
+             smooth=None, splits=0, ws=None, ws_bytes=0, out=FAKE, lse=None)
+    a.update(kw)
+    f = lib.pkv_paged_attn_decode
+    f.restype = ctypes.c_int32
+    return f(ctypes.byref(pool), ctypes.c_void_p(a["q"]), a["B"], a["Hq"],
+             ctypes.c_void_p(a["bt"]), a["max_pages"], ctypes.c_void_p(a["sl"]),
+             a["max_seq_len"], ctypes.c_float(a["scale"]), ctypes.c_void_p(a["smooth"]),
+             a["splits"], ctypes.c_void_p(a["ws"]), ctypes.c_size_t(a["ws_bytes"]),
+             ctypes.c_void_p(a["out"]), ctypes.c_void_p(a["lse"]), None)
+
+
+INVALID, UNSUPPORTED = -1, -2
+
+
+@pytest.mark.parametrize("bad", [dict(head_dim=64), dict(page_size=32), dict(num_kv_heads=0),
+                                 dict(k=None), dict(k=FAKE + 8), dict(dtype=7),
+                                 dict(k_scale=FAKE), dict(dtype=1)])
+def test_decode_rejects_bad_pool(lib, bad):
+    assert decode(lib, good_pool(**bad)) == INVALID
+
+
+@pytest.mark.parametrize("bad", [dict(Hq=3), dict(q=None), dict(out=None), dict(B=-1),
+                                 dict(max_seq_len=65), dict(scale=float("nan")),
+                                 dict(splits=-2), dict(smooth=FAKE)])
+def test_decode_rejects_bad_arguments(lib, bad):
+    assert decode(lib, good_pool(), **bad) == INVALID
+
+
+def test_decode_rejects_short_workspace(lib):
+    # four splits of one page each need a workspace; none given
+    assert decode(lib, good_pool(), splits=4) == INVALID
+    s, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    assert lib.pkv_decode_plan(1, 4, 2, 64, 4, ctypes.byref(s), ctypes.byref(c),
+                               ctypes.byref(w)) == 0
+    assert (s.value, c.value) == (4, 1) and w.value > 0
+    assert decode(lib, good_pool(), splits=4, ws=FAKE, ws_bytes=w.value - 1) == INVALID
+    assert decode(lib, good_pool(), splits=4, ws=FAKE + 16, ws_bytes=w.value) == INVALID
+
+
+def test_decode_unsupported_group_size(lib):
+    assert decode(lib, good_pool(num_kv_heads=1), Hq=3) == UNSUPPORTED
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    assert decode(lib, good_pool(), B=0) == 0
+
+
+def test_plan_heuristic_bounds(lib):
+    s, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    for B, Hkv, L in [(1, 8, 1024), (64, 8, 8192), (1, 8, 32768), (8, 8, 32768), (32, 8, 16398)]:
+        assert lib.pkv_decode_plan(B, 4 * Hkv, Hkv, L, 0, ctypes.byref(s), ctypes.byref(c),
+                                   ctypes.byref(w)) == 0
+        pages = (L + 15) // 16
+        assert 1 <= c.value <= 32 and s.value == -(-pages // c.value)
+        if s.value > 1:
+            assert w.value >= B * 4 * Hkv * s.value * 129 * 4
+        else:
+            assert w.value == 0
+
+
+def test_append_rejects_bad_arguments(lib):
+    f = lib.pkv_kv_append
+    f.restype = ctypes.c_int32
+    p = good_pool()
+    args = [ctypes.byref(p), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), 8,
+            ctypes.c_void_p(FAKE), 1, ctypes.c_void_p(FAKE), 4, ctypes.c_void_p(FAKE), None, None]
+    assert f(*args[:1], None, *args[2:]) == INVALID            # no k_new
+    bad = list(args)
+    bad[9] = ctypes.c_void_p(FAKE)                              # smoothing on a bf16 pool
+    assert f(*bad) == INVALID
+    zero = list(args)
+    zero[3] = 0
+    assert f(*zero) == 0                                        # nothing to append
+
+
+def test_prefill_rejects_int8_pool_and_bad_arguments(lib):
+    f = lib.pkv_paged_attn_prefill
+    f.restype = ctypes.c_int32
+    i8 = good_pool(dtype=1, k_scale=FAKE, v_scale=FAKE)
+    V = ctypes.c_void_p
+    args = [V(FAKE), V(FAKE), 1, 4, V(FAKE), 4, V(FAKE), 16, ctypes.c_float(0.1), V(FAKE),
+            None, None]
+    assert f(ctypes.byref(i8), *args) == UNSUPPORTED
+    bf = good_pool()
+    bad = list(args)
+    bad[3] = 3                                                  # Hq not a multiple of Hkv
+    assert f(ctypes.byref(bf), *bad) == INVALID
+
+
+def test_status_strings(lib):
+    f = lib.pkv_status_string
+    f.restype = ctypes.c_char_p
+    for s in (0, -1, -2, -3, -4):
+        assert f(s)

@@ -1,0 +1,170 @@
+"""paged_attn_decode on the GPU against the fp64 oracle, element by element
+(TileInfer.jl "Performance" page: online softmax over the pages in place,
+split-KV for decode plus a combine; "INT8 KV cache")."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_flash_gb300 import workloads as W
+from tests.helpers import check_lse, check_out, dev, dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_flash_gb300 import pagedkv
+    return pagedkv
+
+
+def gpu_decode(pk, case: W.DecodeCase, num_splits=0, int8_pools=None, smooth=None):
+    if int8_pools is None:
+        pool = pk.Pool(dev_bf16(case.k_pool), dev_bf16(case.v_pool))
+    else:
+        pool = pk.Pool(*[dev(a) for a in int8_pools])
+    out, lse = pk.paged_attn_decode(pool, dev_bf16(case.q), dev(case.layout.block_table),
+                                    dev(case.seq_lens), int(case.seq_lens.max()), case.scale,
+                                    k_smooth=dev(smooth) if smooth is not None else None,
+                                    num_splits=num_splits)
+    assert pk.poll_device_error() == pk.OK
+    return out, lse
+
+
+def oracle_decode(case: W.DecodeCase, rows=None, int8_pools=None, smooth=None):
+    cu = np.arange(case.B + 1, dtype=np.int32)
+    if int8_pools is None:
+        return oracle.paged_attention(case.k_pool, case.v_pool, case.q, cu,
+                                      case.layout.block_table, case.seq_lens, case.scale,
+                                      rows=rows)
+    k8, v8, ks, vs = int8_pools
+    return oracle.paged_attention(k8, v8, case.q, cu, case.layout.block_table, case.seq_lens,
+                                  case.scale, k_scale=ks, v_scale=vs, k_smooth=smooth, rows=rows)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 3, 7, 64])
+def test_single_sequence_1k(pk, splits):
+    case = W.decode_1k()
+    out, lse = gpu_decode(pk, case, splits)
+    ro, rl = oracle_decode(case)
+    check_out(out, ro, f"decode 1k splits={splits}")
+    check_lse(lse, rl, f"decode 1k splits={splits}")
+
+
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_ragged_lengths_and_group_sizes(pk, G):
+    rng = np.random.default_rng(30 + G)
+    lens = [1, 15, 16, 17, 33, 100, 257, 1000, 63, 64, 65]
+    case = W.decode_bf16(rng, lens, Hq=2 * G, Hkv=2)
+    ro, rl = oracle_decode(case)
+    for splits in (0, 1, 5):
+        out, lse = gpu_decode(pk, case, splits)
+        check_out(out, ro, f"G={G} splits={splits}")
+        check_lse(lse, rl, f"G={G} splits={splits}")
+
+
+def test_empty_context_row(pk):
+    rng = np.random.default_rng(40)
+    case = W.decode_bf16(rng, [0, 40, 0], Hq=8, Hkv=2)
+    ro, rl = oracle_decode(case)
+    for splits in (0, 1, 3):
+        out, lse = gpu_decode(pk, case, splits)
+        check_out(out, ro, "empty rows")
+        check_lse(lse, rl, "empty rows")
+
+
+def test_batched_decode_small(pk):
+    case = W.batched_decode(B=8, lo=512, hi=2048)
+    out, lse = gpu_decode(pk, case)
+    ro, rl = oracle_decode(case)
+    check_out(out, ro, "batched small")
+    check_lse(lse, rl, "batched small")
+
+
+def test_batched_decode_64_sequences_sampled(pk):
+    """Full size (64 sequences, lengths 512..8192) in the bench's launch
+    configuration; the oracle evaluates a seeded sample of 16 sequences."""
+    case = W.batched_decode()
+    out, lse = gpu_decode(pk, case)
+    rows = np.sort(np.random.default_rng(41).choice(case.B, 16, replace=False)).astype(np.int32)
+    ro, rl = oracle_decode(case, rows=rows)
+    check_out(out[torch.from_numpy(rows).long().cuda()], ro, "batched full")
+    check_lse(lse[torch.from_numpy(rows).long().cuda()], rl, "batched full")
+
+
+def test_page_permutation_is_bit_identical(pk):
+    rng = np.random.default_rng(42)
+    case = W.decode_bf16(rng, [300, 77, 1024], Hq=32, Hkv=8)
+    out1, lse1 = gpu_decode(pk, case)
+    perm = rng.permutation(case.k_pool.shape[0])
+    kp2 = np.empty_like(case.k_pool)
+    vp2 = np.empty_like(case.v_pool)
+    kp2[perm] = case.k_pool
+    vp2[perm] = case.v_pool
+    case2 = W.DecodeCase(case.Hq, case.Hkv, case.seq_lens,
+                         W.Layout(case.layout.num_pages,
+                                  perm[case.layout.block_table].astype(np.int32),
+                                  int(perm[case.layout.sentinel_page])),
+                         case.q, kp2, vp2)
+    out2, lse2 = gpu_decode(pk, case2)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def int8_case(pk, B, smooth=True):
+    """Fill an INT8 cache of B x 32,768 positions with kv_append, as the
+    workload does, and return (decode case, int8 pools as numpy, w)."""
+    app, q = W.int8_long_decode(B=B)
+    w = app.k_smooth if smooth else None
+    pool = pk.Pool.empty(app.layout.num_pages, app.Hkv, dtype=torch.int8)
+    for t in (pool.k, pool.v):
+        t.fill_(0x5A)
+    for t in (pool.k_scale, pool.v_scale):
+        t.fill_(float("nan"))
+    pk.kv_append(pool, dev_bf16(app.k_new), dev_bf16(app.v_new), dev(app.cu_new),
+                 dev(app.layout.block_table), dev(app.seq_lens),
+                 k_smooth=dev(w) if w is not None else None)
+    assert pk.poll_device_error() == pk.OK
+    pools = tuple(t.cpu().numpy() for t in (pool.k, pool.v, pool.k_scale, pool.v_scale))
+    case = W.DecodeCase(32, app.Hkv, app.seq_lens, app.layout, q, None, None)
+    return case, pools, w
+
+
+@pytest.mark.parametrize("smooth", [True, False])
+def test_int8_32k_batch1(pk, smooth):
+    case, pools, w = int8_case(pk, 1, smooth)
+    ro, rl = oracle_decode(case, int8_pools=pools, smooth=w)
+    for splits in (0, 1, 9):
+        out, lse = gpu_decode(pk, case, splits, int8_pools=pools, smooth=w)
+        check_out(out, ro, f"int8 32k smooth={smooth} splits={splits}")
+        check_lse(lse, rl, f"int8 32k smooth={smooth} splits={splits}")
+
+
+def test_int8_32k_batch8_sampled(pk):
+    case, pools, w = int8_case(pk, 8, True)
+    out, lse = gpu_decode(pk, case, int8_pools=pools, smooth=w)
+    rows = np.array([0, 5], np.int32)
+    ro, rl = oracle_decode(case, rows=rows, int8_pools=pools, smooth=w)
+    idx = torch.from_numpy(rows).long().cuda()
+    check_out(out[idx], ro, "int8 32k b8")
+    check_lse(lse[idx], rl, "int8 32k b8")
+
+
+@pytest.mark.parametrize("G", [1, 2, 8])
+def test_int8_group_sizes_ragged(pk, G):
+    rng = np.random.default_rng(50 + G)
+    lens = np.array([1, 17, 200, 513], np.int32)
+    layout = W.scatter_pages(rng, lens)
+    T = int(lens.sum())
+    w = W.smoothing_weight(rng)
+    app = W.AppendCase(2, W.cu_from_counts(lens), lens, layout,
+                       W.keys_with_channel_weight(rng, (T, 2, W.HEAD_DIM), w),
+                       W.normal_bf16(rng, (T, 2, W.HEAD_DIM)), k_smooth=w)
+    pools = oracle.kv_append_int8(*W.empty_pool_int8(layout.num_pages, 2), app.k_new,
+                                  app.v_new, app.cu_new, layout.block_table, lens, k_smooth=w)
+    q = W.normal_bf16(rng, (4, 2 * G, W.HEAD_DIM))
+    case = W.DecodeCase(2 * G, 2, lens, layout, q, None, None)
+    ro, rl = oracle_decode(case, int8_pools=pools, smooth=w)
+    for splits in (0, 3):
+        out, lse = gpu_decode(pk, case, splits, int8_pools=pools, smooth=w)
+        check_out(out, ro, f"int8 G={G}")
+        check_lse(lse, rl, f"int8 G={G}")

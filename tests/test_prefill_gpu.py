@@ -1,0 +1,145 @@
+"""paged_attn_prefill (tcgen05) on the GPU against the fp64 oracle, element
+by element: causal, chunked against the cached prefix, bottom-right aligned
+(TileInfer.jl "Performance" page: paged flash attention over the pages in
+place; a block per head over every page; chunked prefill)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_flash_gb300 import workloads as W
+from tests.helpers import check_lse, check_out, dev, dev_bf16
+
+pytestmark = pytest.mark.gpu
+D = W.HEAD_DIM
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from paged_kv_flash_gb300 import pagedkv
+    return pagedkv
+
+
+def chunk_case(rng, shapes, Hq, Hkv):
+    """Sequences with (q_len, L): L cached positions of which the last q_len
+    are this chunk's rows.  The pool holds all L positions (NaN elsewhere)."""
+    lens = np.array([L for _, L in shapes], np.int32)
+    case = W.decode_bf16(rng, lens, Hq, Hkv)
+    qlens = [q for q, _ in shapes]
+    q = W.normal_bf16(rng, (sum(qlens), Hq, D))
+    return case, q, W.cu_from_counts(qlens), max(qlens)
+
+
+def run(pk, case, q, cu, max_q):
+    pool = pk.Pool(dev_bf16(case.k_pool), dev_bf16(case.v_pool))
+    out, lse = pk.paged_attn_prefill(pool, dev_bf16(q), dev(cu), dev(case.layout.block_table),
+                                     dev(case.seq_lens), max_q, case.scale)
+    assert pk.poll_device_error() == pk.OK
+    return out, lse
+
+
+def ref(case, q, cu, rows=None):
+    return oracle.paged_attention(case.k_pool, case.v_pool, q, cu, case.layout.block_table,
+                                  case.seq_lens, case.scale, rows=rows)
+
+
+def test_tiny_causal_brute_force(pk):
+    """q_len, L <= 40 with page edges inside the chunk, several sequences."""
+    rng = np.random.default_rng(60)
+    shapes = [(5, 37), (40, 40), (1, 1), (17, 33), (16, 16), (3, 19)]
+    case, q, cu, mq = chunk_case(rng, shapes, Hq=8, Hkv=2)
+    out, lse = run(pk, case, q, cu, mq)
+    ro, rl = ref(case, q, cu)
+    check_out(out, ro, "tiny causal")
+    check_lse(lse, rl, "tiny causal")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (4, 4), (16, 2)])
+def test_ragged_chunks_against_prefix(pk, Hq, Hkv):
+    """Chunks spanning several 128-row tiles and 128-key blocks, ragged tails."""
+    rng = np.random.default_rng(61 + Hq)
+    shapes = [(300, 1000), (129, 129), (128, 700), (257, 260)]
+    case, q, cu, mq = chunk_case(rng, shapes, Hq=Hq, Hkv=Hkv)
+    out, lse = run(pk, case, q, cu, mq)
+    ro, rl = ref(case, q, cu)
+    check_out(out, ro, f"ragged {Hq}/{Hkv}")
+    check_lse(lse, rl, f"ragged {Hq}/{Hkv}")
+
+
+def test_prompt_1024_tokens_after_append(pk):
+    """The 1,024-token prompt: kv_append into seeded pages, then prefill."""
+    app, q = W.prefill_prompt()
+    kp, vp = W.empty_pool_bf16(app.layout.num_pages, app.Hkv)
+    pool = pk.Pool(dev_bf16(kp), dev_bf16(vp))
+    bt, sl = dev(app.layout.block_table), dev(app.seq_lens)
+    pk.kv_append(pool, dev_bf16(app.k_new), dev_bf16(app.v_new), dev(app.cu_new), bt, sl)
+    scale = 1.0 / np.sqrt(D)
+    out, lse = pk.paged_attn_prefill(pool, dev_bf16(q), dev(app.cu_new), bt, sl, 1024, scale)
+    assert pk.poll_device_error() == pk.OK
+    kr, vr = oracle.kv_append_bf16(kp, vp, app.k_new, app.v_new, app.cu_new,
+                                   app.layout.block_table, app.seq_lens)
+    ro, rl = oracle.paged_attention(kr, vr, q, app.cu_new, app.layout.block_table,
+                                    app.seq_lens, scale)
+    check_out(out, ro, "prompt 1024")
+    check_lse(lse, rl, "prompt 1024")
+
+
+def test_page_permutation_is_bit_identical(pk):
+    rng = np.random.default_rng(62)
+    case, q, cu, mq = chunk_case(rng, [(200, 500)], Hq=8, Hkv=2)
+    out1, lse1 = run(pk, case, q, cu, mq)
+    perm = rng.permutation(case.k_pool.shape[0])
+    kp2 = np.empty_like(case.k_pool)
+    vp2 = np.empty_like(case.v_pool)
+    kp2[perm] = case.k_pool
+    vp2[perm] = case.v_pool
+    case2 = W.DecodeCase(case.Hq, case.Hkv, case.seq_lens,
+                         W.Layout(case.layout.num_pages,
+                                  perm[case.layout.block_table].astype(np.int32), 0),
+                         case.q, kp2, vp2)
+    out2, lse2 = run(pk, case2, q, cu, mq)
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+
+
+def test_mixed_step_chunks_sampled(pk):
+    """The 26,926-token prompt in 2,048-row chunks at full size: append every
+    chunk; check all rows of the first chunk and seeded samples of the middle
+    and last (302-row) chunks against the oracle."""
+    wl = W.mixed_step(R=1, lo=128, hi=256)
+    pool = pk.Pool(dev_bf16(wl.k_pool), dev_bf16(wl.v_pool))
+    bt_all = wl.layout.block_table
+    bt = dev(bt_all[:1])
+    kp, vp = wl.k_pool, wl.v_pool
+    scale = 1.0 / np.sqrt(D)
+    rng = np.random.default_rng(63)
+    checks = {0: None, 6: 24, len(wl.steps) - 1: 24}
+    for c, s in enumerate(wl.steps):
+        cu = W.cu_from_counts([s.chunk_len])
+        lens = np.array([s.prefill_len], np.int32)
+        k_new, v_new = s.k_new[:s.chunk_len], s.v_new[:s.chunk_len]
+        pk.kv_append(pool, dev_bf16(k_new), dev_bf16(v_new), dev(cu), bt, dev(lens))
+        kp, vp = oracle.kv_append_bf16(kp, vp, k_new, v_new, cu, bt_all[:1], lens)
+        if c not in checks:
+            continue
+        out, lse = pk.paged_attn_prefill(pool, dev_bf16(s.q_chunk), dev(cu), bt, dev(lens),
+                                         s.chunk_len, scale)
+        assert pk.poll_device_error() == pk.OK
+        n = checks[c]
+        rows = np.arange(s.chunk_len, dtype=np.int32) if n is None else \
+            np.sort(rng.choice(s.chunk_len, n, replace=False)).astype(np.int32)
+        if c == len(wl.steps) - 1:
+            rows = np.unique(np.concatenate([rows, [0, s.chunk_len - 1]])).astype(np.int32)
+        ro, rl = oracle.paged_attention(kp, vp, s.q_chunk, cu, bt_all[:1], lens, scale,
+                                        rows=rows)
+        idx = torch.from_numpy(rows).long().cuda()
+        check_out(out[idx], ro, f"mixed chunk {c}")
+        check_lse(lse[idx], rl, f"mixed chunk {c}")
+
+
+def test_empty_chunk_is_a_no_op(pk):
+    rng = np.random.default_rng(64)
+    case, q, cu, mq = chunk_case(rng, [(0, 40), (8, 40)], Hq=4, Hkv=2)
+    out, lse = run(pk, case, q, cu, mq)
+    ro, rl = ref(case, q, cu)
+    check_out(out, ro, "empty chunk")
+    check_lse(lse, rl, "empty chunk")
