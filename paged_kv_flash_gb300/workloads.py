@@ -35,11 +35,15 @@ def rng_for(workload_index: int, salt: int = 0) -> np.random.Generator:
 
 
 def to_bf16_bits(x) -> np.ndarray:
-    """float32 -> bf16 bit patterns, round to nearest even (inputs are finite)."""
+    """float32 -> bf16 bit patterns, round to nearest even.  Inputs are finite,
+    so the 32-bit sum below cannot wrap (largest: 0xFF7FFFFF + 0x8000)."""
     f = np.ascontiguousarray(x, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return u.astype(np.uint16)
+    u = f.view(np.uint32)
+    r = (u >> 16) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= 16
+    return r.astype(np.uint16)
 
 
 def bits_to_float(b) -> np.ndarray:
