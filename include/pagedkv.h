@@ -137,6 +137,45 @@ pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t ba
                                  size_t workspace_bytes, void* out, float* lse, void* stream);
 
 /*
+ * paged_attn_decode_noalloc -- the same decode as pkv_paged_attn_decode for
+ * callers that cannot allocate device memory.  The pages have no counterpart
+ * for this call: it exists for users of this library, not for the method.
+ *
+ * Some callers have no way to obtain the workspace the split partials need:
+ * a plain C host program that has no device allocator of its own, a plugin
+ * running inside a runtime that owns every byte of device memory and forbids
+ * cudaMalloc on its threads (cudaMalloc can synchronise the device and
+ * fragments the runtime's pool), or latency-critical code that cannot afford
+ * an allocation's implicit synchronisation.  This entry point keeps the
+ * partials in a fixed device array that lives in the library itself (16 MiB,
+ * 256-byte aligned; every GPU that loads the library holds it until the
+ * process exits) and calls no cudaMalloc, cudaFree or other allocating
+ * routine.  The caller still passes q, the pool, the tables and out/lse.
+ *
+ * Arguments: as pkv_paged_attn_decode, without the workspace.  With
+ * num_splits == 0 the split heuristic runs first; if its partials would not
+ * fit in 16 MiB the split count is lowered until they do (the result differs
+ * from pkv_paged_attn_decode only by rounding).  A forced num_splits whose
+ * partials need more than 16 MiB (batch * num_q_heads * num_splits * 516 bytes
+ * plus alignment) is rejected with PKV_ERR_INVALID before any launch.
+ *
+ * The first call on each device looks the array's device address up with
+ * cudaGetSymbolAddress (once per device, with that device current); make
+ * that first call before any stream capture on the device.  Every call on a
+ * device shares the one array and it keeps the last call's contents; nothing
+ * in it needs to start at zero (every entry the combine reads is written by
+ * the split kernel of the same call).  Calls that overlap on the GPU -- on
+ * two streams, or from two host threads without ordering -- race on the
+ * array and give wrong results: order them on one stream.
+ */
+pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, int32_t batch,
+                                         int32_t num_q_heads, const int32_t* block_table,
+                                         int32_t max_pages, const int32_t* seq_lens,
+                                         int32_t max_seq_len, float softmax_scale,
+                                         const float* k_smooth, int32_t num_splits, void* out,
+                                         float* lse, void* stream);
+
+/*
  * paged_attn_prefill -- causal attention of a chunk of new query rows per
  * sequence against the sequence's cached prefix plus the chunk itself
  * (a block of query rows per head over every page: "Attention for verify

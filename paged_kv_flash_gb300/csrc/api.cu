@@ -178,6 +178,67 @@ pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t ba
                                              static_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, int32_t batch,
+                                         int32_t num_q_heads, const int32_t* block_table,
+                                         int32_t max_pages, const int32_t* seq_lens,
+                                         int32_t max_seq_len, float softmax_scale,
+                                         const float* k_smooth, int32_t num_splits, void* out,
+                                         float* lse, void* stream) {
+  // Same checks as pkv_paged_attn_decode; the split partials go to the
+  // library's fixed device array instead of a caller workspace.
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads || max_pages <= 0 ||
+      max_seq_len < 0 || (long long)max_seq_len > (long long)max_pages * pkv::kPageSize ||
+      num_splits < 0 || !std::isfinite(softmax_scale))
+    return PKV_ERR_INVALID;
+  if (!pkv_host::decode_supports_group(num_q_heads / pool->num_kv_heads))
+    return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (!q || !block_table || !seq_lens || !out) return PKV_ERR_INVALID;
+  if (pool->dtype == PKV_BF16 && k_smooth) return PKV_ERR_INVALID;
+  const size_t cap = pkv_host::decode_fixed_scratch_bytes();
+  Plan p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, num_splits);
+  if (p.ws_bytes > cap) {
+    if (num_splits > 0) return PKV_ERR_INVALID;       // forced split count does not fit
+    int s = p.splits;
+    while (s > 1 && p.ws_bytes > cap) {
+      --s;
+      p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, s);
+    }
+    if (p.ws_bytes > cap) return PKV_ERR_INVALID;
+  }
+  if ((long long)batch > 65535) return PKV_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (p.ws_bytes > 0 && pkv_host::decode_fixed_scratch(&scratch) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  pkv_host::DecodeLaunch a{};
+  a.k = pool->k;
+  a.v = pool->v;
+  a.k_scale = pool->k_scale;
+  a.v_scale = pool->v_scale;
+  a.num_pages = pool->num_pages;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.q = q;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.softmax_scale = softmax_scale;
+  a.k_smooth = k_smooth;
+  a.splits = p.splits;
+  a.pages_per_split = p.pages_per_split;
+  a.ws_o = p.ws_bytes ? static_cast<float*>(scratch) : nullptr;
+  a.ws_lse = p.ws_bytes
+                 ? reinterpret_cast<float*>(static_cast<char*>(scratch) + p.ws_lse_offset)
+                 : nullptr;
+  a.out = out;
+  a.lse = lse;
+  return cuda_status(pkv_host::launch_decode(a, pool->dtype == PKV_INT8,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, const int32_t* cu_q,
                                   int32_t batch, int32_t num_q_heads,
                                   const int32_t* block_table, int32_t max_pages,

@@ -25,6 +25,7 @@
 // lse; with a single split the kernel writes the bf16 output directly and
 // the combine is skipped.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -545,6 +546,42 @@ uint32_t take_decode_error(cudaStream_t s) {
   if (h) cudaMemcpyToSymbolAsync(g_err_decode, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
   cudaStreamSynchronize(s);
   return h;
+}
+
+}  // namespace pkv_host
+
+// ------------------------------------------------------------------------
+// Fixed scratch for callers that cannot allocate (pkv_paged_attn_decode_noalloc).
+// It holds the split partials that pkv_paged_attn_decode keeps in the
+// caller's workspace.  In host code the name below is only a stand-in for
+// the device array, never a device address: the kernels receive the address
+// that cudaGetSymbolAddress returns for the current device.
+
+static constexpr size_t kFixedScratchBytes = size_t(16) << 20;   // 16 MiB
+static __device__ __align__(256) unsigned char g_decode_fixed_scratch[kFixedScratchBytes];
+
+namespace pkv_host {
+
+size_t decode_fixed_scratch_bytes() { return kFixedScratchBytes; }
+
+cudaError_t decode_fixed_scratch(void** ptr) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_fixed_scratch);
+    if (e != cudaSuccess) return e;
+    if (!p) return cudaErrorInvalidSymbol;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace pkv_host

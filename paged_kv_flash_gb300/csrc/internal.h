@@ -56,6 +56,12 @@ bool decode_supports_group(int group);
 cudaError_t launch_decode(const DecodeLaunch& a, bool int8, cudaStream_t s);
 uint32_t take_decode_error(cudaStream_t s);
 
+// Fixed device scratch for pkv_paged_attn_decode_noalloc (decode.cu).
+size_t decode_fixed_scratch_bytes();
+// Device address of that scratch on the current device (looked up once per
+// device with cudaGetSymbolAddress).
+cudaError_t decode_fixed_scratch(void** ptr);
+
 struct PrefillLaunch {
   const void* k;
   const void* v;

@@ -47,6 +47,8 @@ SIGNATURES = {
                              ctypes.POINTER(_SZ)]),
     "pkv_paged_attn_decode": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P, _SZ,
                                    _P, _P, _P]),
+    "pkv_paged_attn_decode_noalloc": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P,
+                                           _P, _P]),
     "pkv_paged_attn_prefill": (_I, [_POOLP, _P, _P, _I, _I, _P, _I, _P, _I, _F, _P, _P, _P]),
     "pkv_poll_device_error": (_I, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
@@ -181,6 +183,30 @@ def paged_attn_decode(pool: Pool, q, block_table, seq_lens, max_seq_len, softmax
         int(num_splits), _ptr(workspace), workspace.numel() if workspace is not None else 0,
         _ptr(out), _ptr(lse), _stream(stream))
     _check(st, "pkv_paged_attn_decode")
+    return out, lse
+
+
+def paged_attn_decode_noalloc(pool: Pool, q, block_table, seq_lens, max_seq_len, softmax_scale,
+                              k_smooth=None, num_splits=0, out=None, lse=None, want_lse=True,
+                              stream=None):
+    """Decode for callers that cannot allocate device memory: the split
+    partials live in the library's fixed 16 MiB device array instead of a
+    workspace (see pkv_paged_attn_decode_noalloc).  Calls on one device share
+    that array, so they must not overlap on the GPU."""
+    _need(q, torch.bfloat16, "q")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    B, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    pc = pool.c()
+    st = _lib.pkv_paged_attn_decode_noalloc(
+        ctypes.byref(pc), _ptr(q), B, Hq, _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), int(max_seq_len), float(softmax_scale), _ptr(k_smooth),
+        int(num_splits), _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "pkv_paged_attn_decode_noalloc")
     return out, lse
 
 
