@@ -46,20 +46,24 @@ constexpr int BN = 128;                       // keys per block (8 pages)
 constexpr int NSTAGE = 2;                     // K and V ring depth
 constexpr int HALF = 16384;                   // one 128 x 64 bf16 swizzled half-tile
 constexpr int TILE = 2 * HALF;                // 128 x 128 bf16
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 320;              // softmax A: warps 0-3, B: 4-7, TMA 8, MMA 9
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_O = 256;                // O accumulator columns 256..383
+// TMEM columns: S_A 0..127, S_B 128..255, O_A 256..383, O_B 384..511.  P of a
+// tile (bf16 pairs, 64 columns) overwrites the upper half of its S columns.
+__host__ __device__ constexpr uint32_t tm_s(int x) { return (uint32_t)x * 128u; }
+__host__ __device__ constexpr uint32_t tm_o(int x) { return 256u + (uint32_t)x * 128u; }
+__host__ __device__ constexpr uint32_t tm_p(int x) { return (uint32_t)x * 128u + 64u; }
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE;
+constexpr int OFF_Q = 0;                      // Q_A, Q_B
+constexpr int OFF_K = OFF_Q + 2 * TILE;
 constexpr int OFF_V = OFF_K + NSTAGE * TILE;
-constexpr int OFF_P = OFF_V + NSTAGE * TILE;
-constexpr int OFF_BAR = OFF_P + TILE;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2],
-// s_free[2], p_full, pv_done, drain
+constexpr int OFF_BAR = OFF_V + NSTAGE * TILE;
+// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[A,B],
+// p_full[A,B], o_done[A,B], drain
 constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 3, BAR_VF = 5, BAR_VE = 7, BAR_SF = 9,
-              BAR_SR = 11, BAR_PF = 13, BAR_PV = 14, BAR_DR = 15, NUM_BARS = 16;
+              BAR_PF = 11, BAR_OD = 13, BAR_DR = 15, NUM_BARS = 16;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
 
@@ -136,6 +140,52 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+#define PKV_R16(i) PKV_R8(i), PKV_R8(i + 8)
+#define PKV_W16(i) PKV_W8(i), PKV_W8(i + 8)
+
+// 64 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,"
+      "%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,"
+      "%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : PKV_R16(0), PKV_R16(16), PKV_R16(32), PKV_R16(48)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,"
+      "%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,"
+      "%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};"
+      ::"r"(taddr), PKV_W16(0), PKV_W16(16), PKV_W16(32), PKV_W16(48)
+      : "memory");
+}
+
+// D (TMEM) (+)= A (TMEM, 128 lanes x 16 bf16 in 8 columns) * B (shared).
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (lo, hi) -> bf16x2 with lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
   asm volatile(
@@ -143,11 +193,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 // Bounded wait shared by all roles; the result is uniform across the warp.
@@ -173,7 +218,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 struct PrefillParams {
   pkv_host::PrefillLaunch a;
-  int n_tiles;                  // tiles of the longest chunk
+  int n_pairs;                  // pairs of 128-row tiles of the longest chunk
 };
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -181,7 +226,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const __grid_constant__ PrefillParams prm) {
   const pkv_host::PrefillLaunch& a = prm.a;
   const int hq = blockIdx.x;
-  const int t = prm.n_tiles - 1 - (int)blockIdx.y;      // heaviest tiles first
+  const int pair = prm.n_pairs - 1 - (int)blockIdx.y;   // heaviest tiles first
   const int b = blockIdx.z;
   const int Hq = a.num_q_heads;
   const int G = Hq / a.num_kv_heads;
@@ -189,18 +234,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int q0 = a.cu_q[b];
   const int q_len = a.cu_q[b + 1] - q0;
-  if (q_len > prm.n_tiles * BM && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+  if (q_len > prm.n_pairs * 2 * BM && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
     atomicOr(&g_err_prefill, kErrBadIndex);             // chunk longer than max_q_len
-  if (t * BM >= q_len) return;                          // no rows in this tile
+  const int row0 = pair * 2 * BM;                       // first chunk row of tile A
+  if (row0 >= q_len) return;                            // no rows in this pair
   const int L = a.seq_lens[b];
   if (L < q_len || L > a.max_pages * kPageSize) {
     if (threadIdx.x == 0) atomicOr(&g_err_prefill, kErrBadIndex);
     return;
   }
-  const int pos_min = L - q_len + t * BM;                     // position of tile row 0
-  const int rows = min(BM, q_len - t * BM);
-  const int pos_max = pos_min + rows - 1;
-  const int n_blk = pos_max / BN + 1;
+  // tile x (0 = A, 1 = B): rows row0 + x*128 .. ; positions L - q_len + row
+  auto rows_of = [&](int x) { return max(0, min(BM, q_len - row0 - x * BM)); };
+  auto pmin_of = [&](int x) { return L - q_len + row0 + x * BM; };
+  auto nblk_of = [&](int x) {
+    const int rws = rows_of(x);
+    return rws > 0 ? (pmin_of(x) + rws - 1) / BN + 1 : 0;
+  };
+  const int nblk_a = nblk_of(0), nblk_b = nblk_of(1);
+  const int n_blk = max(nblk_a, nblk_b);
   const int npages = (L + kPageSize - 1) / kPageSize;
 
   extern __shared__ uint8_t smem_raw[];
@@ -213,24 +264,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(bar(BAR_Q), 128);
+    mbar_init(bar(BAR_Q), 2 * BM);
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(bar(BAR_KF + s), 1);
       mbar_init(bar(BAR_KE + s), 1);
       mbar_init(bar(BAR_VF + s), 1);
       mbar_init(bar(BAR_VE + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(BAR_SF + s), 1);
-      mbar_init(bar(BAR_SR + s), 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(BAR_SF + x), 1);
+      mbar_init(bar(BAR_PF + x), BM);
+      mbar_init(bar(BAR_OD + x), 1);
     }
-    mbar_init(bar(BAR_PF), 128);
-    mbar_init(bar(BAR_PV), 1);
     mbar_init(bar(BAR_DR), 1);
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == WARP_MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(smem_u32(tmem_slot)), "r"(TMEM_COLS) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -240,9 +290,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  int last_k[NSTAGE], last_v[NSTAGE];            // producer: last block issued per stage
-  for (int s = 0; s < NSTAGE; ++s) last_k[s] = last_v[s] = -1;
-  if (warp == 0) {
+  static_assert(NSTAGE == 2, "the producer tracks two stages");
+  int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;   // last block issued per stage
+  if (warp == WARP_TMA) {
     // ------------------------------------------------------ TMA producer
     const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
     bool ok = true;
@@ -257,9 +307,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           pg = 0;
         }
       }
-      int pgs[8];
+      // lanes 0..7 hold the block's page ids; lane 0 needs them all
+      int rowk[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
+      for (int i = 0; i < 8; ++i)
+        rowk[i] = (__shfl_sync(0xffffffffu, pg, i) * a.num_kv_heads + hkv) * kPageSize;
       const int nload = min(BN / kPageSize, npages - j * (BN / kPageSize));
       const uint32_t bytes = (uint32_t)nload * 2u * (kPageSize * 64 * 2);
       if (j >= NSTAGE && !(ok = wait_bar(bar(BAR_KE + st), ((j / NSTAGE) - 1) & 1, abort_flag)))
@@ -267,102 +319,124 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(BAR_KF + st), bytes);
         const uint32_t dst = base_s + OFF_K + st * TILE;
-        for (int i = 0; i < nload; ++i) {
-          const int row = (pgs[i] * a.num_kv_heads + hkv) * kPageSize;
-          tma_load_2d(dst + i * 2048, &tk, 0, row, bar(BAR_KF + st));
-          tma_load_2d(dst + HALF + i * 2048, &tk, 64, row, bar(BAR_KF + st));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i < nload) {
+            tma_load_2d(dst + i * 2048, &tk, 0, rowk[i], bar(BAR_KF + st));
+            tma_load_2d(dst + HALF + i * 2048, &tk, 64, rowk[i], bar(BAR_KF + st));
+          }
         }
       }
-      last_k[st] = j;
+      (st == 0 ? last_k0 : last_k1) = j;
       if (j >= NSTAGE && !(ok = wait_bar(bar(BAR_VE + st), ((j / NSTAGE) - 1) & 1, abort_flag)))
         break;
       if (lane == 0) {
         mbar_arrive_expect_tx(bar(BAR_VF + st), bytes);
         const uint32_t dst = base_s + OFF_V + st * TILE;
-        for (int i = 0; i < nload; ++i) {
-          const int row = (pgs[i] * a.num_kv_heads + hkv) * kPageSize;
-          tma_load_2d(dst + i * 2048, &tv, 0, row, bar(BAR_VF + st));
-          tma_load_2d(dst + HALF + i * 2048, &tv, 64, row, bar(BAR_VF + st));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i < nload) {
+            tma_load_2d(dst + i * 2048, &tv, 0, rowk[i], bar(BAR_VF + st));
+            tma_load_2d(dst + HALF + i * 2048, &tv, 64, rowk[i], bar(BAR_VF + st));
+          }
         }
       }
-      last_v[st] = j;
+      (st == 0 ? last_v0 : last_v1) = j;
     }
-  } else if (warp == 1) {
+  } else if (warp == WARP_MMA) {
     // ------------------------------------------------------- MMA issuer
-    auto pv = [&](int jj) -> bool {
-      const int st = jj % NSTAGE;
-      if (!wait_bar(bar(BAR_PF), jj & 1, abort_flag)) return false;
-      if (!wait_bar(bar(BAR_VF + st), (jj / NSTAGE) & 1, abort_flag)) return false;
-      const int kbase = jj * BN;
-      if (kbase + BN > L) {
-        // zero V rows at positions >= L (both 64-channel halves of each row)
-        const int first = L - kbase;
-        uint8_t* vt = base + OFF_V + st * TILE;
-        for (int idx = lane; idx < (BN - first) * 16; idx += 32) {
-          const int row = first + (idx >> 4), c = idx & 15;
-          *reinterpret_cast<uint4*>(vt + (c >> 3) * HALF + row * 128 + (c & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-        fence_async_smem();
-        __syncwarp();
-      }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t p_s = base_s + OFF_P, v_s = base_s + OFF_V + st * TILE;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16(tmem + TM_O, desc_kmajor(p_s + (kk >> 2) * HALF + (kk & 3) * 32),
-                   desc_mnmajor(v_s + kk * 2048), IDESC_PV, (jj > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(BAR_PV));
-        mma_commit(bar(BAR_VE + st));
-      }
-      __syncwarp();
-      return true;
-    };
+    // Iteration j: PV_A(j-1), QK_A(j), PV_B(j-1), QK_B(j).  While softmax A
+    // works on S_A(j) the tensor core runs PV_B(j-1) and QK_B(j), and the
+    // other way round.  QK_x(j) overwrites S_x, which holds P_x(j-1): it is
+    // issued after PV_x(j-1), and MMAs of one thread run in issue order.
     bool ok = wait_bar(bar(BAR_Q), 0, abort_flag);
-    for (int j = 0; j < n_blk && ok; ++j) {
-      const int st = j % NSTAGE;
-      if (!(ok = wait_bar(bar(BAR_KF + st), (j / NSTAGE) & 1, abort_flag))) break;
-      if (j >= 2 && !(ok = wait_bar(bar(BAR_SR + (j & 1)), ((j - 2) >> 1) & 1, abort_flag))) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t q_s = base_s + OFF_Q, k_s = base_s + OFF_K + st * TILE;
-#pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-          mma_bf16(tmem + (j & 1) * BN, desc_kmajor(q_s + off), desc_kmajor(k_s + off), IDESC_QK,
-                   kk > 0 ? 1u : 0u);
+    for (int j = 0; j <= n_blk && ok; ++j) {
+      const bool has_qk = j < n_blk;
+      const int st = j % NSTAGE, pst = (j + NSTAGE - 1) % NSTAGE;
+      if (has_qk && !(ok = wait_bar(bar(BAR_KF + st), (j / NSTAGE) & 1, abort_flag))) break;
+      if (j >= 1) {
+        if (!(ok = wait_bar(bar(BAR_VF + pst), ((j - 1) / NSTAGE) & 1, abort_flag))) break;
+        const int kbase = (j - 1) * BN;
+        if (kbase + BN > L) {
+          // zero V rows at positions >= L (both 64-channel halves of each row)
+          const int first = L - kbase;
+          uint8_t* vt = base + OFF_V + pst * TILE;
+          for (int idx = lane; idx < (BN - first) * 16; idx += 32) {
+            const int row = first + (idx >> 4), c = idx & 15;
+            *reinterpret_cast<uint4*>(vt + (c >> 3) * HALF + row * 128 + (c & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+          __syncwarp();
         }
-        mma_commit(bar(BAR_SF + (j & 1)));
-        mma_commit(bar(BAR_KE + st));
+      }
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int nbx = x == 0 ? nblk_a : nblk_b;
+        if (j >= 1 && j - 1 < nbx) {
+          if (!(ok = wait_bar(bar(BAR_PF + x), (j - 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t v_s = base_s + OFF_V + pst * TILE;
+#pragma unroll 1
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_bf16_tmem_a(tmem + tm_o(x), tmem + tm_p(x) + 8 * kk,
+                              desc_mnmajor(v_s + kk * 2048), IDESC_PV,
+                              (j > 1 || kk > 0) ? 1u : 0u);
+            if (j - 1 == nbx - 1) mma_commit(bar(BAR_OD + x));
+          }
+          __syncwarp();
+        }
+        if (has_qk && j < nbx) {
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t q_s = base_s + OFF_Q + x * TILE, k_s = base_s + OFF_K + st * TILE;
+#pragma unroll 1
+            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+              mma_bf16(tmem + tm_s(x), desc_kmajor(q_s + off), desc_kmajor(k_s + off), IDESC_QK,
+                       kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bar(BAR_SF + x));
+          }
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        if (has_qk) mma_commit(bar(BAR_KE + st));
+        if (j >= 1) mma_commit(bar(BAR_VE + pst));
       }
       __syncwarp();
-      if (j >= 1) ok = pv(j - 1);
     }
-    if (ok) ok = pv(n_blk - 1);
     // drain: every MMA issued above completes before TMEM is released
     if (lane == 0) mma_commit(bar(BAR_DR));
     __syncwarp();
     (void)mbar_wait(bar(BAR_DR), 0);
   } else {
     // ---------------------------------------------------------- softmax
+    const int x = warp >> 2;                      // tile: 0 = A, 1 = B
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;            // row of the tile
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int rows = rows_of(x);
+    const int pos_min = pmin_of(x);
+    const int n_x = x == 0 ? nblk_a : nblk_b;
     const int pos_r = min(pos_min + r, L - 1);    // padding rows clamp to the last key
     const bool row_valid = r < rows;
+    const int qrow0 = q0 + row0 + x * BM;         // chunk row of tile row 0
 
     // Q tile -> swizzled shared memory (rows past the chunk are zero).
     {
       const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-      uint8_t* qs = base + OFF_Q;
+      uint8_t* qs = base + OFF_Q + x * TILE;
       for (int it = 0; it < 16; ++it) {
         const int row = quarter * 32 + 2 * it + (lane >> 4);
         const int c = lane & 15;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (row < rows)
           v = __ldg(reinterpret_cast<const uint4*>(
-                        qg + ((size_t)(q0 + t * BM + row) * Hq + hq) * kHeadDim) + c);
+                        qg + ((size_t)(qrow0 + row) * Hq + hq) * kHeadDim) + c);
         *reinterpret_cast<uint4*>(qs + (c >> 3) * HALF + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
             v;
       }
@@ -371,127 +445,130 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 
     const float sl2 = a.softmax_scale * kLog2e;
-    float m_run = -INFINITY, l_run = 0.f;
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    float m_run = -INFINITY, l_run = 0.f;        // running max (scaled, log2 domain), sum
     bool ok = true;
-    for (int j = 0; j < n_blk; ++j) {
-      if (!(ok = wait_bar(bar(BAR_SF + (j & 1)), (j >> 1) & 1, abort_flag))) break;
+    for (int j = 0; j < n_x; ++j) {
+      if (!(ok = wait_bar(bar(BAR_SF + x), j & 1, abort_flag))) break;
       tc_fence_after();
-      float s[BN];
-#pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(t_lane + (j & 1) * BN + 32 * c, rr);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(BAR_SR + (j & 1)));
-
+      // S row in two 64-column halves: pass 1 takes the row max; pass 2 turns
+      // the upper half (still in registers) into P columns 96..127, then
+      // reloads the lower half and writes P columns 64..95 -- P only ever
+      // overwrites S columns that are already consumed.
       const int kbase = j * BN;
+      const bool diag = kbase + BN - 1 > pos_min;   // block crosses the causal edge
+      const int lim = pos_r - kbase;
+      uint32_t sr[64];
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (kbase + BN - 1 > pos_min) {               // block crosses the causal edge
-        const int lim = pos_r - kbase;
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          s[c] = (c > lim) ? -INFINITY : s[c] * sl2;
-          mx[c & 3] = fmaxf(mx[c & 3], s[c]);
-        }
-      } else {
+      for (int h = 0; h < 2; ++h) {
+        tmem_ld64(t_lane + tm_s(x) + 64 * h, sr);
+        tmem_wait_ld();
+        if (diag) {
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          s[c] *= sl2;
-          mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+          for (int c = 0; c < 64; ++c)
+            if (64 * h + c > lim) sr[c] = __float_as_uint(-INFINITY);
         }
+#pragma unroll
+        for (int c = 0; c < 64; c += 2)
+          mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sr[c]),
+                                   __uint_as_float(sr[c + 1]));
       }
-      const float m_blk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float m_blk = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
       const float m_new = fmaxf(m_run, m_blk);
-      const bool need = m_new > m_run + 8.0f;       // lazy rescale threshold (2^8)
+      const bool need = m_new > m_run + 8.0f;     // lazy rescale threshold (2^8)
       const float m_use = need ? m_new : m_run;
       const float alpha = need ? fast_exp2(m_run - m_use) : 1.0f;
-      uint32_t pk[BN / 2];
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      const float2 negm = make_float2(-m_use, -m_use);
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 1
+      for (int h = 1; h >= 0; --h) {
+        if (h == 0) {
+          tmem_ld64(t_lane + tm_s(x), sr);
+          tmem_wait_ld();
+          if (diag) {
 #pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = fast_exp2(s[2 * c] - m_use);
-        const float p1 = fast_exp2(s[2 * c + 1] - m_use);
-        sum[c & 3] += p0 + p1;
-        pk[c] = pack_bf16(p0, p1);
+            for (int c = 0; c < 64; ++c)
+              if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+          }
+        }
+        // packed P overwrites the S registers it came from (c <= 2c)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float2 t = fma2(make_float2(__uint_as_float(sr[2 * c]),
+                                            __uint_as_float(sr[2 * c + 1])), sl2x2, negm);
+          const float2 pp = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+          sum2[c & 1] = add2(sum2[c & 1], pp);
+          sr[c] = pack_bf16x2(pp.x, pp.y);
+        }
+        tmem_st32(t_lane + tm_p(x) + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
       }
-      l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      const float2 s2 = add2(sum2[0], sum2[1]);
+      l_run = l_run * alpha + (s2.x + s2.y);
       m_run = m_use;
 
-      if (j > 0) {
-        // PV of the previous block must be done: the P buffer is free and O
-        // holds every earlier block.
-        if (!(ok = wait_bar(bar(BAR_PV), (j - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
+      // O rescale: S_x(j) complete implies PV_x(j-1) complete (one thread
+      // issues both, in order), so O_x is stable here.
+      if (j > 0 && __any_sync(0xffffffffu, need)) {
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          uint32_t o[32];
+          tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < kHeadDim / 32; ++c) {
-            uint32_t rr[32];
-            tmem_ld32(t_lane + TM_O + 32 * c, rr);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-            tmem_st32(t_lane + TM_O + 32 * c, rr);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 v = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+            o[i] = __float_as_uint(v.x);
+            o[i + 1] = __float_as_uint(v.y);
           }
-          tmem_wait_st();
+          tmem_st32(t_lane + tm_o(x) + 32 * h, o);
         }
       }
-      // P row -> swizzled K-major shared tile (16-byte chunk c of a 128-byte
-      // row lands at chunk c ^ (row & 7)).
-      uint8_t* ps = base + OFF_P;
-#pragma unroll
-      for (int ch = 0; ch < BN / 8; ++ch) {
-        *reinterpret_cast<uint4*>(ps + (ch >> 3) * HALF + r * 128 + (((ch & 7) ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      }
-      fence_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(BAR_PF));
+      mbar_arrive(bar(BAR_PF + x));
     }
 
-    if (ok && wait_bar(bar(BAR_PV), (n_blk - 1) & 1, abort_flag)) {
+    if (ok && n_x > 0 && wait_bar(bar(BAR_OD + x), 0, abort_flag)) {
       tc_fence_after();
       const float inv = 1.0f / l_run;
-      const size_t orow = ((size_t)(q0 + t * BM + r) * Hq + hq) * kHeadDim;
+      const size_t orow = ((size_t)(qrow0 + r) * Hq + hq) * kHeadDim;
       uint4* og = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
-#pragma unroll
-      for (int c = 0; c < kHeadDim / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(t_lane + TM_O + 32 * c, rr);
+#pragma unroll 1
+      for (int h = 0; h < 4; ++h) {
+        uint32_t o[32];
+        tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
         tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             uint4 v;
-            v.x = pack_bf16(__uint_as_float(rr[8 * k + 0]) * inv, __uint_as_float(rr[8 * k + 1]) * inv);
-            v.y = pack_bf16(__uint_as_float(rr[8 * k + 2]) * inv, __uint_as_float(rr[8 * k + 3]) * inv);
-            v.z = pack_bf16(__uint_as_float(rr[8 * k + 4]) * inv, __uint_as_float(rr[8 * k + 5]) * inv);
-            v.w = pack_bf16(__uint_as_float(rr[8 * k + 6]) * inv, __uint_as_float(rr[8 * k + 7]) * inv);
-            og[4 * c + k] = v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+            og[4 * h + k] = v;
           }
         }
       }
       if (row_valid && a.lse)
-        a.lse[(size_t)(q0 + t * BM + r) * Hq + hq] = (m_run + fast_log2(l_run)) * kLn2;
+        a.lse[(size_t)(qrow0 + r) * Hq + hq] = (m_run + fast_log2(l_run)) * kLn2;
     }
   }
 
   // Every role has left its loop.  After an abort, loads may still be in
   // flight: the producer lets each one land before the CTA can exit.
   __syncthreads();
-  if (warp == 0 && *abort_flag) {
-    for (int s = 0; s < NSTAGE; ++s) {
-      if (last_k[s] >= 0) (void)mbar_wait(bar(BAR_KF + s), (last_k[s] / NSTAGE) & 1);
-      if (last_v[s] >= 0) (void)mbar_wait(bar(BAR_VF + s), (last_v[s] / NSTAGE) & 1);
-    }
+  if (warp == WARP_TMA && *abort_flag) {
+    if (last_k0 >= 0) (void)mbar_wait(bar(BAR_KF + 0), (last_k0 / NSTAGE) & 1);
+    if (last_k1 >= 0) (void)mbar_wait(bar(BAR_KF + 1), (last_k1 / NSTAGE) & 1);
+    if (last_v0 >= 0) (void)mbar_wait(bar(BAR_VF + 0), (last_v0 / NSTAGE) & 1);
+    if (last_v1 >= 0) (void)mbar_wait(bar(BAR_VF + 1), (last_v1 / NSTAGE) & 1);
   }
-
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == WARP_MMA) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
                  : "memory");
@@ -549,8 +626,8 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  PrefillParams prm{a, (a.max_q_len + BM - 1) / BM};
-  dim3 grid(a.num_q_heads, prm.n_tiles, a.batch);
+  PrefillParams prm{a, (a.max_q_len + 2 * BM - 1) / (2 * BM)};
+  dim3 grid(a.num_q_heads, prm.n_pairs, a.batch);
   prefill_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tk, tv, prm);
   return cudaGetLastError();
 }
