@@ -173,6 +173,66 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
       ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
+// Eight back-to-back MMAs over K = 128 (one 128-column block) in one asm
+// block, so the issuing warp spends about three instructions per MMA even
+// when the softmax warps keep its scheduler busy.  Descriptor start
+// addresses advance by immediates (16-byte units): K-major 128B-swizzled
+// tiles step 32 B within a 128-byte row, then jump to the second 64-column
+// half 16 KiB on; the MN-major V tile steps 16 keys = 2 KiB.
+#define PKV_MMA_SS(acc) \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, " acc ";\n\t"
+__device__ __forceinline__ void mma8_qk(uint32_t d_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      "mov.b64 ra, %1;\n\tmov.b64 rb, %2;\n\t" PKV_MMA_SS("pf")
+      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 2;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 4;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 6;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 1024;\n\tadd.s64 rb, %2, 1024;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 1026;\n\tadd.s64 rb, %2, 1026;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 1028;\n\tadd.s64 rb, %2, 1028;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 1030;\n\t" PKV_MMA_SS("pt")
+      "}"
+      ::"r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc));
+}
+// P (K-major, shared) x V (MN-major, shared); the first MMA accumulates iff acc0.
+__device__ __forceinline__ void mma8_pv_ss(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                           uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p0, pt;\n\t.reg .b64 ra, rb;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      "mov.b64 ra, %1;\n\tmov.b64 rb, %2;\n\t" PKV_MMA_SS("p0")
+      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 128;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 256;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 384;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 1024;\n\tadd.s64 rb, %2, 512;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 1026;\n\tadd.s64 rb, %2, 640;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 1028;\n\tadd.s64 rb, %2, 768;\n\t" PKV_MMA_SS("pt")
+      "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 896;\n\t" PKV_MMA_SS("pt")
+      "}"
+      ::"r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "r"(acc0));
+}
+#define PKV_MMA_TS(acc) \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %3, " acc ";\n\t"
+// P (TMEM, 8 columns per 16 keys) x V (MN-major, shared).
+__device__ __forceinline__ void mma8_pv_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                           uint32_t idesc, uint32_t acc0) {
+  asm volatile(
+      "{\n\t.reg .pred p0, pt;\n\t.reg .b32 ta;\n\t.reg .b64 rb;\n\t"
+      "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+      "mov.b32 ta, %1;\n\tmov.b64 rb, %2;\n\t" PKV_MMA_TS("p0")
+      "add.u32 ta, %1, 8;\n\tadd.s64 rb, %2, 128;\n\t" PKV_MMA_TS("pt")
+      "add.u32 ta, %1, 16;\n\tadd.s64 rb, %2, 256;\n\t" PKV_MMA_TS("pt")
+      "add.u32 ta, %1, 24;\n\tadd.s64 rb, %2, 384;\n\t" PKV_MMA_TS("pt")
+      "add.u32 ta, %1, 32;\n\tadd.s64 rb, %2, 512;\n\t" PKV_MMA_TS("pt")
+      "add.u32 ta, %1, 40;\n\tadd.s64 rb, %2, 640;\n\t" PKV_MMA_TS("pt")
+      "add.u32 ta, %1, 48;\n\tadd.s64 rb, %2, 768;\n\t" PKV_MMA_TS("pt")
+      "add.u32 ta, %1, 56;\n\tadd.s64 rb, %2, 896;\n\t" PKV_MMA_TS("pt")
+      "}"
+      ::"r"(d_tmem), "r"(a_tmem), "l"(b0), "r"(idesc), "r"(acc0));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -378,11 +438,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           if (lane == 0) {
             const uint32_t v_s = base_s + OFF_V + pst * TILE;
-#pragma unroll 1
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_bf16_tmem_a(tmem + tm_o(x), tmem + tm_p(x) + 8 * kk,
-                              desc_mnmajor(v_s + kk * 2048), IDESC_PV,
-                              (j > 1 || kk > 0) ? 1u : 0u);
+            mma8_pv_ts(tmem + tm_o(x), tmem + tm_p(x), desc_mnmajor(v_s), IDESC_PV,
+                       j > 1 ? 1u : 0u);
             if (j - 1 == nbx - 1) mma_commit(bar(BAR_OD + x));
           }
           __syncwarp();
@@ -391,12 +448,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           if (lane == 0) {
             const uint32_t q_s = base_s + OFF_Q + x * TILE, k_s = base_s + OFF_K + st * TILE;
-#pragma unroll 1
-            for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-              mma_bf16(tmem + tm_s(x), desc_kmajor(q_s + off), desc_kmajor(k_s + off), IDESC_QK,
-                       kk > 0 ? 1u : 0u);
-            }
+            mma8_qk(tmem + tm_s(x), desc_kmajor(q_s), desc_kmajor(k_s), IDESC_QK);
             mma_commit(bar(BAR_SF + x));
           }
           __syncwarp();
@@ -451,29 +503,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int j = 0; j < n_x; ++j) {
       if (!(ok = wait_bar(bar(BAR_SF + x), j & 1, abort_flag))) break;
       tc_fence_after();
-      // S row in two 64-column halves: pass 1 takes the row max; pass 2 turns
-      // the upper half (still in registers) into P columns 96..127, then
-      // reloads the lower half and writes P columns 64..95 -- P only ever
-      // overwrites S columns that are already consumed.
+      // The whole S row in one round trip (two 64-column loads, one wait);
+      // packed P then overwrites the S registers it came from (c <= 2c) and
+      // goes to TMEM columns 64..127 of S_x, which are consumed by then.
       const int kbase = j * BN;
-      const bool diag = kbase + BN - 1 > pos_min;   // block crosses the causal edge
-      const int lim = pos_r - kbase;
-      uint32_t sr[64];
+      uint32_t sr[128];
+      tmem_ld64(t_lane + tm_s(x), *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
+      tmem_ld64(t_lane + tm_s(x) + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
+      tmem_wait_ld();
+      if (kbase + BN - 1 > pos_min) {             // block crosses the causal edge
+        const int lim = pos_r - kbase;
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+      }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tmem_ld64(t_lane + tm_s(x) + 64 * h, sr);
-        tmem_wait_ld();
-        if (diag) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (64 * h + c > lim) sr[c] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int c = 0; c < 64; c += 2)
-          mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sr[c]),
-                                   __uint_as_float(sr[c + 1]));
-      }
+      for (int c = 0; c < BN; c += 2)
+        mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sr[c]),
+                                 __uint_as_float(sr[c + 1]));
       const float m_blk = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
       const float m_new = fmaxf(m_run, m_blk);
       const bool need = m_new > m_run + 8.0f;     // lazy rescale threshold (2^8)
@@ -481,28 +529,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float alpha = need ? fast_exp2(m_run - m_use) : 1.0f;
       const float2 negm = make_float2(-m_use, -m_use);
       float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 1
-      for (int h = 1; h >= 0; --h) {
-        if (h == 0) {
-          tmem_ld64(t_lane + tm_s(x), sr);
-          tmem_wait_ld();
-          if (diag) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-          }
-        }
-        // packed P overwrites the S registers it came from (c <= 2c)
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 t = fma2(make_float2(__uint_as_float(sr[2 * c]),
-                                            __uint_as_float(sr[2 * c + 1])), sl2x2, negm);
-          const float2 pp = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-          sum2[c & 1] = add2(sum2[c & 1], pp);
-          sr[c] = pack_bf16x2(pp.x, pp.y);
-        }
-        tmem_st32(t_lane + tm_p(x) + 32 * h, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+      for (int c = 0; c < BN / 2; ++c) {
+        const float2 t = fma2(make_float2(__uint_as_float(sr[2 * c]),
+                                          __uint_as_float(sr[2 * c + 1])), sl2x2, negm);
+        const float2 pp = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+        sum2[c & 1] = add2(sum2[c & 1], pp);
+        sr[c] = pack_bf16x2(pp.x, pp.y);
       }
+      tmem_st64(t_lane + tm_p(x), *reinterpret_cast<const uint32_t(*)[64]>(&sr[0]));
       const float2 s2 = add2(sum2[0], sum2[1]);
       l_run = l_run * alpha + (s2.x + s2.y);
       m_run = m_use;
