@@ -52,11 +52,17 @@ pkv_status check_pool(const pkv_pool* pool) {
 // Split plan: pages per split C and split count S for a decode call.
 //
 // The split kernel runs one CTA per (split, KV head, sequence) with 4 warps,
-// two CTAs resident per SM.  The heuristic aims for about eight waves of
-// CTAs, estimated from the longest sequence, so that sequences of unequal
-// length balance across the SMs; a split covers 4 to 32 pages (64 to 512
-// positions) and C is a multiple of the 4 warps so that they get equal work.
-// A forced split count S gives C = ceil(pages / S).
+// two CTAs resident per SM.  A CTA pays a few microseconds of start-up
+// (query and block-table loads, the first page copies), so splits are made
+// as long as the machine allows: about 0.8 CTAs per resident slot, estimated
+// from the longest sequence, with 8 to 128 pages (128 to 2,048 positions) per
+// split, a multiple of the 4 warps so that they get equal work.  Measured on
+// GB300: 64 sequences of 512..8,192 positions run best at 64..128 pages per
+// split; one 32k-position INT8 sequence at 64; eight of them at 128.  A
+// forced split count S gives C = ceil(pages / S).
+constexpr long long kPlanSlotsNum = 4, kPlanSlotsDen = 5;   // 0.8 CTAs per slot
+constexpr long long kPlanMinPages = 8, kPlanMaxPages = 128;
+
 struct Plan {
   int splits, pages_per_split;
   size_t ws_bytes, ws_lse_offset;
@@ -70,8 +76,9 @@ Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, in
   } else {
     const long long slots = (long long)sm_count() * pkv_host::kDecodeCtasPerSm;
     const long long page_heads = (long long)batch * num_kv_heads * mp;
-    long long c = (page_heads + 8 * slots - 1) / (8 * slots);
-    c = std::max<long long>(4, std::min<long long>(32, c));
+    const long long target = std::max<long long>(1, slots * kPlanSlotsNum / kPlanSlotsDen);
+    long long c = (page_heads + target - 1) / target;
+    c = std::max<long long>(kPlanMinPages, std::min<long long>(kPlanMaxPages, c));
     c = (c + pkv_host::kDecodeWarps - 1) / pkv_host::kDecodeWarps * pkv_host::kDecodeWarps;
     C = (int)std::min<long long>(c, mp);
   }

@@ -260,34 +260,6 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
   }
   __syncwarp();
 
-  // Query rows of the group, pre-scaled by softmax_scale * log2(e) (and by
-  // the key smoothing weight, which the dequantised keys carry).
-  WarpState<G, INT8> st;
-  {
-    const float qs = a.softmax_scale * kLog2e;
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const __nv_bfloat16* qrow = qb + ((size_t)b * Hq + h * G + g) * kHeadDim;
-#pragma unroll
-      for (int j = 0; j < C::NLD; ++j) {
-        const int jj = (j + kg) & (C::NLD - 1);
-        const int d0 = dl * C::DPL + jj * C::EPL;
-#pragma unroll
-        for (int i = 0; i < C::EPL / 2; ++i) {
-          float x0 = __bfloat162float(qrow[d0 + 2 * i]) * qs;
-          float x1 = __bfloat162float(qrow[d0 + 2 * i + 1]) * qs;
-          if (INT8 && a.k_smooth) {
-            x0 *= __ldg(a.k_smooth + d0 + 2 * i);
-            x1 *= __ldg(a.k_smooth + d0 + 2 * i + 1);
-          }
-          st.q[j][i][g] = make_float2(x0, x1);
-          st.o[j][i][g] = make_float2(0.f, 0.f);
-        }
-      }
-    }
-  }
-
   const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
   const size_t Hkv = (size_t)a.num_kv_heads;
   const uint8_t* kpool = static_cast<const uint8_t*>(a.k);
@@ -332,6 +304,40 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
   const int pro = min(NBUF, n_w);
   for (int i = 0; i < pro; ++i) issue(i, page_id(i));
   int issued = pro;
+  // Query rows of the group, pre-scaled by softmax_scale * log2(e) (and by
+  // the key smoothing weight, which the dequantised keys carry).  Loaded
+  // after the first page copies are in flight, so their latency overlaps.
+  WarpState<G, INT8> st;
+  {
+    const float qs = a.softmax_scale * kLog2e;
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const __nv_bfloat16* qrow = qb + ((size_t)b * Hq + h * G + g) * kHeadDim;
+#pragma unroll
+      for (int j = 0; j < C::NLD; ++j) {
+        const int jj = (j + kg) & (C::NLD - 1);
+        const int d0 = dl * C::DPL + jj * C::EPL;      // EPL is 8 or 16: whole 16-byte chunks
+#pragma unroll
+        for (int c8 = 0; c8 < C::EPL / 8; ++c8) {
+          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8 * c8));
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x0 = bf16lo(w[e]) * qs, x1 = bf16hi(w[e]) * qs;
+            if (INT8 && a.k_smooth) {
+              const float2 ww = __ldg(reinterpret_cast<const float2*>(a.k_smooth + d0 + 8 * c8 + 2 * e));
+              x0 *= ww.x;
+              x1 *= ww.y;
+            }
+            st.q[j][4 * c8 + e][g] = make_float2(x0, x1);
+            st.o[j][4 * c8 + e][g] = make_float2(0.f, 0.f);
+          }
+        }
+      }
+    }
+  }
+
   bool failed = false;
   int i_fail = 0;
   for (int i = 0; i < n_w; ++i) {

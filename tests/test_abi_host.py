@@ -115,7 +115,7 @@ def test_plan_heuristic_bounds(lib):
         assert lib.pkv_decode_plan(B, 4 * Hkv, Hkv, L, 0, ctypes.byref(s), ctypes.byref(c),
                                    ctypes.byref(w)) == 0
         pages = (L + 15) // 16
-        assert 1 <= c.value <= 32 and s.value == -(-pages // c.value)
+        assert 1 <= c.value <= 128 and s.value == -(-pages // c.value)
         if s.value > 1:
             assert w.value >= B * 4 * Hkv * s.value * 129 * 4
         else:
