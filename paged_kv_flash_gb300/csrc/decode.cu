@@ -38,7 +38,9 @@ __device__ uint32_t g_err_decode;
 
 template <int G, bool INT8>
 struct Cfg {
-  static constexpr int DL = (G <= 2) ? 4 : (G == 4 ? 8 : 16);   // lanes per key
+  // lanes per key: INT8 with G = 4 uses 16 lanes (8 channels each), which
+  // halves the query/accumulator registers so more warps fit per SM
+  static constexpr int DL = (G <= 2) ? 4 : ((G == 4 && !INT8) ? 8 : 16);
   static constexpr int KG = 32 / DL;                              // keys per pass
   static constexpr int PASSES = kPageSize / KG;
   static constexpr int DPL = kHeadDim / DL;                       // channels per lane
@@ -51,7 +53,7 @@ struct Cfg {
   static constexpr int SCB = INT8 ? kPageSize * 4 : 0;            // scale bytes per slab
   static constexpr int BUF = 2 * SLAB + 2 * SCB;                  // one page of K, V (+scales)
   static constexpr int HL = DL / G;                               // lanes per head after scatter
-  static constexpr int NBUF = INT8 ? 5 : 3;                       // page buffers per warp
+  static constexpr int NBUF = INT8 ? (DL == 16 ? 3 : 5) : 3;      // page buffers per warp
   static_assert(NLD >= 1 && (NLD & (NLD - 1)) == 0, "loads per key must be a power of two");
   static_assert(BUF % 128 == 0, "page buffers stay 128-byte aligned");
 };
