@@ -36,6 +36,16 @@ sys.path.insert(0, ROOT)
 
 from paged_kv_flash_gb300 import workloads as W  # noqa: E402
 
+# DRAM bytes (read + write) per prefill launch of the mixed step, from one ncu
+# capture of `bench.py --profile-case prefill_chunk` (2,048 rows against
+# 16,384 positions: 148.9 MB, profiles/prefill_kernel_chunk2048_ctx16384.md),
+# scaled to the mixed step's average context per launch (15,235 positions):
+# K/V traffic grows with the context a chunk attends to.  Re-measure (or set
+# to None) whenever the prefill kernel changes.
+PREFILL_TRAFFIC_BYTES = 138.5e6
+PREFILL_TRAFFIC_NOTE = ("ncu dram read+write of a 2,048 x 16,384 launch (148.9 MB) scaled by "
+                        "mean context 15,235 / 16,384")
+
 METRIC = ("decode attn µs & HBM GB/s (% of 8 TB/s); prefill attn TFLOP/s (% of peak)")
 NOMINAL_HBM_GBS = 8000.0
 D = W.HEAD_DIM
@@ -473,6 +483,67 @@ def cpu_baseline(mixed_wl, budget_s=20.0):
                        f"(row, head, key) triples")}
 
 
+# ------------------------------------------------------- profiling cases
+
+def profile_case(torch, pk, name, reps=3):
+    """One kernel on a fixed, seeded workload, launched `reps` times (for ncu
+    captures of a single launch: -k <kernel> -s 2 -c 1).  Prints the CUDA-event
+    time of an extra 10 launches."""
+    rng = np.random.default_rng(5)
+    if name == "prefill_chunk":
+        qlen, L = 2048, 16384
+        case = W.decode_bf16(rng, [L], 32, 8)
+        q = to_dev_bf16(torch, W.normal_bf16(rng, (qlen, 32, D)))
+        pool = pk.Pool(to_dev_bf16(torch, case.k_pool), to_dev_bf16(torch, case.v_pool))
+        cu, bt, sl = (to_dev(torch, W.cu_from_counts([qlen])), to_dev(torch, case.layout.block_table),
+                      to_dev(torch, case.seq_lens))
+        out = torch.empty_like(q)
+        lse = torch.empty((qlen, 32), dtype=torch.float32, device="cuda")
+        fn = lambda: pk.paged_attn_prefill(pool, q, cu, bt, sl, qlen, SCALE, out=out, lse=lse)
+        work = prefill_flops(qlen, L, 32)
+        unit = "TFLOP/s"
+    elif name in ("decode_bf16", "decode_int8"):
+        if name == "decode_bf16":
+            case = W.batched_decode(B=16)
+            pool = pk.Pool(to_dev_bf16(torch, case.k_pool), to_dev_bf16(torch, case.v_pool))
+            w, per = None, 512
+        else:
+            app, qh = W.int8_long_decode(B=2)
+            pool = pk.Pool.empty(app.layout.num_pages, app.Hkv, dtype=torch.int8)
+            w = to_dev(torch, app.k_smooth)
+            pk.kv_append(pool, to_dev_bf16(torch, app.k_new), to_dev_bf16(torch, app.v_new),
+                         to_dev(torch, app.cu_new), to_dev(torch, app.layout.block_table),
+                         to_dev(torch, app.seq_lens), k_smooth=w)
+            case = W.DecodeCase(32, app.Hkv, app.seq_lens, app.layout, qh, None, None)
+            per = 264
+        q = to_dev_bf16(torch, case.q)
+        bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
+        ms = int(case.seq_lens.max())
+        _, _, wsb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(q)
+        lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
+        fn = lambda: pk.paged_attn_decode(pool, q, bt, sl, ms, SCALE, k_smooth=w, workspace=ws,
+                                          out=out, lse=lse)
+        work = decode_bytes(case.seq_lens, case.Hkv, per)
+        unit = "GB/s"
+    else:
+        raise SystemExit(f"unknown profile case {name}")
+    for _ in range(reps):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(10):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 100.0
+    rate = work / us / (1e6 if unit == "TFLOP/s" else 1e3)
+    assert pk.poll_device_error() == pk.OK
+    print(json.dumps({"profile_case": name, "us": round(us, 2), unit: round(rate, 1)}))
+
+
 # ---------------------------------------------------------------- main
 
 def main():
@@ -483,6 +554,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["prefill_chunk", "decode_bf16", "decode_int8"],
+                    help="run one kernel on a fixed workload (for ncu) and exit")
     args = ap.parse_args()
     K, Wu = args.steps, max(3, args.warmup)
 
@@ -543,6 +616,9 @@ def main():
         torch.cuda.set_device(0)
     from paged_kv_flash_gb300 import pagedkv as pk
 
+    if args.profile_case:
+        profile_case(torch, pk, args.profile_case)
+        return 0
     hbm, bf16, bf16_sus, peak_src = peaks()
     mixed = Mixed(torch, pk)
     r = time_mixed(torch, pk, mixed, K, Wu, world, rank)
@@ -570,7 +646,8 @@ def main():
         "append": {"us_per_step": round(r["app_ms"] * 1e3 / K, 2)},
         "roofline": {"kernel": "prefill_kernel (tcgen05)", "bound": "tensor",
                      "achieved": round(pre_tflops, 1), "peak": bf16_sus, "unit": "TFLOP/s",
-                     "frac": round(frac, 4), "traffic": None,
+                     "frac": round(frac, 4), "traffic": PREFILL_TRAFFIC_BYTES,
+                     "traffic_note": PREFILL_TRAFFIC_NOTE,
                      "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)",
                      "achieved_note": ("causal flops 4*D*Hq*keys per launch / CUDA-event "
                                        "duration of the prefill launches in the timed region")},
