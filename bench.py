@@ -42,9 +42,8 @@ from paged_kv_flash_gb300 import workloads as W  # noqa: E402
 # scaled to the mixed step's average context per launch (15,235 positions):
 # K/V traffic grows with the context a chunk attends to.  Re-measure (or set
 # to None) whenever the prefill kernel changes.
-PREFILL_TRAFFIC_BYTES = 138.5e6
-PREFILL_TRAFFIC_NOTE = ("ncu dram read+write of a 2,048 x 16,384 launch (148.9 MB) scaled by "
-                        "mean context 15,235 / 16,384")
+PREFILL_TRAFFIC_BYTES = None      # not yet captured for the persistent prefill kernel
+PREFILL_TRAFFIC_NOTE = "ncu dram read+write not yet taken for the current prefill kernel"
 
 METRIC = ("decode attn µs & HBM GB/s (% of 8 TB/s); prefill attn TFLOP/s (% of peak)")
 NOMINAL_HBM_GBS = 8000.0
@@ -180,6 +179,7 @@ class Mixed:
             self.steps.append(st)
         ws_max = max(pk.decode_plan(self.R, wl.Hq, wl.Hkv, s["max_dec"])[2] for s in self.steps)
         self.ws = torch.empty(max(ws_max, 256), dtype=torch.uint8, device="cuda")
+        self.ws_p = pk.prefill_workspace()
         T = max(s["chunk_len"] for s in self.steps)
         self.out_p = torch.empty((T, wl.Hq, D), dtype=torch.bfloat16, device="cuda")
         self.lse_p = torch.empty((T, wl.Hq), dtype=torch.float32, device="cuda")
@@ -198,7 +198,8 @@ class Mixed:
         pk.kv_append(self.pool, x["k_new"], x["v_new"], st["cu_app"], self.bt_all, st["lens_app"])
         if ev: ev[1].record()
         pk.paged_attn_prefill(self.pool, x["q_chunk"], st["cu_q"], self.bt_prompt, st["lens_p"],
-                              n, SCALE, out=self.out_p[:n], lse=self.lse_p[:n])
+                              n, SCALE, workspace=self.ws_p, out=self.out_p[:n],
+                              lse=self.lse_p[:n])
         if ev: ev[2].record()
         pk.paged_attn_decode(self.pool, x["q_dec"], self.bt_dec, st["lens_d"], st["max_dec"],
                              SCALE, workspace=self.ws, out=self.out_d, lse=self.lse_d)
@@ -393,7 +394,9 @@ def other_configs(torch, pk, hbm, bf16):
     lse = torch.empty((1024, 32), dtype=torch.float32, device="cuda")
     ap = lambda: pk.kv_append(pool, kn, vn, cu, bt, sl)
     ap()
-    pf = lambda: pk.paged_attn_prefill(pool, qd, cu, bt, sl, 1024, SCALE, out=out, lse=lse)
+    ws_p = pk.prefill_workspace()
+    pf = lambda: pk.paged_attn_prefill(pool, qd, cu, bt, sl, 1024, SCALE, workspace=ws_p, out=out,
+                                       lse=lse)
     a_med, _ = time_events(torch, ap, flush=flush)
     p_med, p_min = time_events(torch, pf, flush=flush)
     fl = prefill_flops(1024, 1024, 32)
@@ -499,7 +502,9 @@ def profile_case(torch, pk, name, reps=3):
                       to_dev(torch, case.seq_lens))
         out = torch.empty_like(q)
         lse = torch.empty((qlen, 32), dtype=torch.float32, device="cuda")
-        fn = lambda: pk.paged_attn_prefill(pool, q, cu, bt, sl, qlen, SCALE, out=out, lse=lse)
+        ws_p = pk.prefill_workspace()
+        fn = lambda: pk.paged_attn_prefill(pool, q, cu, bt, sl, qlen, SCALE, workspace=ws_p,
+                                           out=out, lse=lse)
         work = prefill_flops(qlen, L, 32)
         unit = "TFLOP/s"
     elif name in ("decode_bf16", "decode_int8"):

@@ -176,6 +176,14 @@ pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, in
                                          float* lse, void* stream);
 
 /*
+ * prefill_plan -- the persistent CTA count, workspace size and the size of
+ * the workspace's leading part that must be zero before first use, for a
+ * prefill call on the current device (one CTA per SM; host only, no GPU
+ * work).  Any pointer may be NULL.  Always PKV_OK.
+ */
+pkv_status pkv_prefill_plan(int32_t* ctas, size_t* workspace_bytes, size_t* zero_bytes);
+
+/*
  * paged_attn_prefill -- causal attention of a chunk of new query rows per
  * sequence against the sequence's cached prefix plus the chunk itself
  * (a block of query rows per head over every page: "Attention for verify
@@ -183,21 +191,36 @@ pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, in
  * QK^T and PV with fp32 accumulation; P is rounded to bf16 for PV.
  *
  *  q         bf16 [total_q][num_q_heads][128]; rows cu_q[b] .. cu_q[b+1]-1
- *            belong to sequence b.  cu_q int32 [batch+1] (device).
+ *            belong to sequence b (all within 0 .. total_q-1).  cu_q int32
+ *            [batch+1] (device).  total_q (host) is the row count of q and
+ *            out.
  *  seq_lens  int32 [batch] cached positions INCLUDING this chunk (append the
  *            chunk's K/V first).  Row i of sequence b sits at position
  *            seq_lens[b] - q_b + i and sees keys 0 .. that position
  *            (bottom-right causal alignment).
  *  max_q_len (host) >= every q_b.
+ *  workspace device scratch of at least pkv_prefill_plan's workspace_bytes,
+ *            16-byte aligned, owned by the caller.  Its first zero_bytes
+ *            bytes (part counters) must be zero before its first use; every
+ *            call that completes leaves them zero again, so a workspace is
+ *            zeroed once and reused (zero it again after PKV_ERR_TIMEOUT).
+ *            The call runs one persistent CTA per SM over an even share of
+ *            all (sequence, query-tile pair, head, key block) work; a unit of
+ *            work cut between CTAs leaves its parts there, and the CTA that
+ *            finishes the last part merges them (the log-sum-exp rule of
+ *            "Split-KV decoding").  PKV_ERR_INVALID if NULL, unaligned or
+ *            too small.  Calls that share a workspace must not overlap.
  *  out       bf16 [total_q][num_q_heads][128]; lse fp32 [total_q][num_q_heads]
  *            or NULL.
  * bf16 pools only (PKV_ERR_UNSUPPORTED for INT8).
  */
-pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, const int32_t* cu_q,
+pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, int32_t total_q,
+                                  const int32_t* cu_q,
                                   int32_t batch, int32_t num_q_heads,
                                   const int32_t* block_table, int32_t max_pages,
                                   const int32_t* seq_lens, int32_t max_q_len,
-                                  float softmax_scale, void* out, float* lse, void* stream);
+                                  float softmax_scale, void* workspace, size_t workspace_bytes,
+                                  void* out, float* lse, void* stream);
 
 /*
  * Synchronises the stream, then reports and clears the device-side error

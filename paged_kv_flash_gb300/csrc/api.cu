@@ -246,24 +246,38 @@ pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, in
                                              static_cast<cudaStream_t>(stream)));
 }
 
-pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, const int32_t* cu_q,
+pkv_status pkv_prefill_plan(int32_t* ctas, size_t* workspace_bytes, size_t* zero_bytes) {
+  const int n = pkv_host::prefill_ctas(sm_count());
+  if (ctas) *ctas = n;
+  if (workspace_bytes) *workspace_bytes = pkv_host::prefill_workspace_bytes(n);
+  if (zero_bytes) *zero_bytes = pkv_host::prefill_workspace_zero_bytes(n);
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, int32_t total_q,
+                                  const int32_t* cu_q,
                                   int32_t batch, int32_t num_q_heads,
                                   const int32_t* block_table, int32_t max_pages,
                                   const int32_t* seq_lens, int32_t max_q_len,
-                                  float softmax_scale, void* out, float* lse, void* stream) {
+                                  float softmax_scale, void* workspace, size_t workspace_bytes,
+                                  void* out, float* lse, void* stream) {
   pkv_status st = check_pool(pool);
   if (st != PKV_OK) return st;
-  if (batch < 0 || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads || max_pages <= 0 ||
-      max_q_len < 0 || !std::isfinite(softmax_scale))
+  if (batch < 0 || total_q < 0 || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads ||
+      max_pages <= 0 || max_q_len < 0 || !std::isfinite(softmax_scale))
     return PKV_ERR_INVALID;
   if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
-  if (batch == 0 || max_q_len == 0) return PKV_OK;
+  if (batch == 0 || max_q_len == 0 || total_q == 0) return PKV_OK;
   if (!q || !cu_q || !block_table || !seq_lens || !out) return PKV_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(out, 16)) return PKV_ERR_INVALID;
   if (batch > 65535 || num_q_heads > 65535) return PKV_ERR_UNSUPPORTED;
-  pkv_host::PrefillLaunch a{pool->k, pool->v, pool->num_pages, pool->num_kv_heads, q, cu_q,
-                            batch, num_q_heads, block_table, max_pages, seq_lens, max_q_len,
-                            softmax_scale, out, lse};
+  const int ctas = pkv_host::prefill_ctas(sm_count());
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < pkv_host::prefill_workspace_bytes(ctas))
+    return PKV_ERR_INVALID;
+  pkv_host::PrefillLaunch a{pool->k, pool->v, pool->num_pages, pool->num_kv_heads, q, total_q,
+                            cu_q, batch, num_q_heads, block_table, max_pages, seq_lens, max_q_len,
+                            softmax_scale, out, lse, ctas, workspace};
   cudaError_t e = pkv_host::launch_prefill(a, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
   return cuda_status(e);

@@ -67,6 +67,7 @@ struct PrefillLaunch {
   const void* v;
   int num_pages, num_kv_heads;
   const void* q;           // bf16 [total_q][Hq][128]
+  int total_q;
   const int32_t* cu_q;     // [B+1]
   int batch, num_q_heads;
   const int32_t* block_table;
@@ -76,8 +77,20 @@ struct PrefillLaunch {
   float softmax_scale;
   void* out;
   float* lse;
+  int ctas;                // persistent CTAs (one per SM)
+  void* workspace;         // prefill_workspace_bytes(ctas) bytes, 16-byte aligned
 };
 
+constexpr int kMaxPrefillCtas = 1024;
+// Workspace of a prefill launch with `ctas` persistent CTAs: part counters,
+// then per CTA two partial-result slots of 256 rows x 128 fp32 plus 256 fp32
+// lse.  Its first prefill_workspace_zero_bytes(ctas) bytes (the counters)
+// must be zero before the first launch; a launch that completes leaves them
+// zero.
+size_t prefill_workspace_bytes(int ctas);
+size_t prefill_workspace_zero_bytes(int ctas);
+// Persistent CTAs of a prefill launch on a device with `sms` SMs.
+int prefill_ctas(int sms);
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s);
 uint32_t take_prefill_error(cudaStream_t s);
 

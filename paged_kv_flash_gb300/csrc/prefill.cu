@@ -4,27 +4,37 @@
 // The method: TileInfer.jl "Performance" page -- paged flash attention runs
 // an online softmax over the pages read in place through the block table
 // ("Fused kernels, FlashAttention and PagedAttention"); the prefill kernel
-// runs a block per head over every page ("Attention for verify steps");
-// chunked prefill attends a chunk of new rows to the cached prefix ("What is
-// left to gain").  Rows sit bottom-right: row i of a chunk of q rows in a
-// sequence of L cached positions is position L - q + i and sees keys 0..it.
+// runs a block of query rows per head over every page ("Attention for verify
+// steps"); chunked prefill attends a chunk of new rows to the cached prefix
+// ("What is left to gain").  Rows sit bottom-right: row i of a chunk of q
+// rows in a sequence of L cached positions is position L - q + i and sees
+// keys 0..it.
 //
-// One CTA per (query head, 128-row query tile, sequence); 6 warps:
-//   warp 0     TMA producer: 128-key K and V blocks, each gathered as eight
-//              16-row page boxes (one per page named by the block table) per
-//              64-channel half, 128-byte swizzled, 2-stage ring per operand;
-//   warp 1     MMA issuer (one thread): S = Q K^T into TMEM (double
-//              buffered, 2 x 128 columns), O += P V into TMEM (128 columns);
-//   warps 2-5  softmax: thread = query row = TMEM lane; reads S with
-//              tcgen05.ld, keeps the running max and sum of its row, rescales
-//              O in TMEM only when its max grows by more than 2^8 (exact: the
-//              final normalisation uses the same stale max), writes P as bf16
-//              into shared memory in the swizzled K-major layout the PV MMA
-//              reads, and finally normalises O and writes out and lse.
-// Q is loaded once by the softmax warps (rows past the chunk are zero) into
-// the same swizzled layout.  V rows at positions >= L in the last block are
-// zeroed by the MMA warp before the PV MMA, so stale or poisoned pool slots
-// can never reach the accumulator (P is 0 there, but 0 * NaN is NaN).
+// Persistent kernel, one CTA per SM, 10 warps:
+//   warps 0-3  softmax of query tile A, warps 4-7 of tile B (thread = query
+//              row = TMEM lane): read S with tcgen05.ld, keep the running
+//              max and sum of the row, write P (bf16) back into TMEM over the
+//              consumed half of S, rescale O in TMEM only when the max grows
+//              by more than 2^8 (exact: the final normalisation uses the same
+//              stale max), and finish each unit of work;
+//   warp 8     producer and scheduler: walks this CTA's share of the work,
+//              publishes one descriptor per segment in a 2-entry shared ring,
+//              and loads Q tiles (TMA, per segment) and 128-key K and V blocks
+//              (TMA, eight 16-row page boxes per 64-channel half, 128-byte
+//              swizzled, 2-stage ring per operand);
+//   warp 9     MMA issuer (one thread): S_x = Q_x K^T and O_x += P_x V for the
+//              two tiles in ping-pong, so that the tensor core works on one
+//              tile while the softmax warps work on the other.
+// V rows at positions >= L in the last block are zeroed before the PV MMA,
+// so stale or poisoned pool slots never reach the accumulator (P is 0 there,
+// but 0 * NaN is NaN).
+//
+// Work split: see "Work decomposition" below.  A unit of work cut between
+// CTAs is finished by whichever of its CTAs completes its part last: each
+// part is written (normalised O, log2-domain lse) to the caller's workspace,
+// a per-unit counter in the workspace counts the parts, and the last one
+// merges them with the log-sum-exp rule ("Split-KV decoding") and resets the
+// counter to zero for the next call.
 //
 // Every wait is bounded (wall clock, one second); a wait that runs out sets
 // the device error word and an abort flag that makes every role leave its
@@ -47,6 +57,11 @@ constexpr int NSTAGE = 2;                     // K and V ring depth
 constexpr int HALF = 16384;                   // one 128 x 64 bf16 swizzled half-tile
 constexpr int TILE = 2 * HALF;                // 128 x 128 bf16
 constexpr int NUM_THREADS = 320;              // softmax A: warps 0-3, B: 4-7, TMA 8, MMA 9
+// Work is measured in tile-blocks (one 128 x 128 QK^T and PV of one tile).
+// A unit also costs kUnitCost0 for starting and finishing it (Q load,
+// pipeline fill and drain, epilogue), and each CTA gets at least kMinCost.
+constexpr int kUnitCost0 = 4;
+constexpr int kMinCost = 2 * kUnitCost0;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S_A 0..127, S_B 128..255, O_A 256..383, O_B 384..511.  P of a
@@ -60,12 +75,21 @@ constexpr int OFF_Q = 0;                      // Q_A, Q_B
 constexpr int OFF_K = OFF_Q + 2 * TILE;
 constexpr int OFF_V = OFF_K + NSTAGE * TILE;
 constexpr int OFF_BAR = OFF_V + NSTAGE * TILE;
-// barriers: q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[A,B],
-// p_full[A,B], o_done[A,B], drain
-constexpr int BAR_Q = 0, BAR_KF = 1, BAR_KE = 3, BAR_VF = 5, BAR_VE = 7, BAR_SF = 9,
-              BAR_PF = 11, BAR_OD = 13, BAR_DR = 15, NUM_BARS = 16;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+// barriers (pairs are per tile or per ring stage): q_full, q_empty, k_full,
+// k_empty, v_full, v_empty, s_full, p_full, o_done, drain, seg_full,
+// seg_empty, and per tile for a cut unit: epi (the tile's 4 warps are done
+// with the part), mrg (the tile's leader has counted it), st (the part is
+// stored), go (every other part is stored: merge)
+constexpr int BAR_QF = 0, BAR_QE = 2, BAR_KF = 4, BAR_KE = 6, BAR_VF = 8, BAR_VE = 10,
+              BAR_SF = 12, BAR_PF = 14, BAR_OD = 16, BAR_DR = 18, BAR_SEGF = 19,
+              BAR_SEGE = 21, BAR_EPI = 23, BAR_MRG = 25, BAR_ST = 27, BAR_GO = 29,
+              NUM_BARS = 31;
+constexpr int NSEG = 2;                       // segment descriptor ring depth
+constexpr int OFF_SEG = OFF_BAR + 256;        // after the barriers (27 x 8 bytes)
+constexpr int OFF_MISC = OFF_SEG + NSEG * 64;
+constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;   // + alignment slack
+static_assert(NUM_BARS * 8 <= 256, "barrier area");
+constexpr int SLOT_ROWS = 2 * BM;             // rows of one workspace slot (both tiles)
 
 // kind::f16 instruction descriptor: D fp32, A and B bf16, M = N = 128.
 // bits 4-5 D format, 7-9 A format, 10-12 B format, 15/16 A/B major
@@ -87,15 +111,6 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) {
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(HALF >> 4) << 16) |
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -163,16 +178,6 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
       : "memory");
 }
 
-// D (TMEM) (+)= A (TMEM, 128 lanes x 16 bf16 in 8 columns) * B (shared).
-__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                                uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-      ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
-}
-
 // Eight back-to-back MMAs over K = 128 (one 128-column block) in one asm
 // block, so the issuing warp spends about three instructions per MMA even
 // when the softmax warps keep its scheduler busy.  Descriptor start
@@ -195,23 +200,6 @@ __device__ __forceinline__ void mma8_qk(uint32_t d_tmem, uint64_t a0, uint64_t b
       "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 1030;\n\t" PKV_MMA_SS("pt")
       "}"
       ::"r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc));
-}
-// P (K-major, shared) x V (MN-major, shared); the first MMA accumulates iff acc0.
-__device__ __forceinline__ void mma8_pv_ss(uint32_t d_tmem, uint64_t a0, uint64_t b0,
-                                           uint32_t idesc, uint32_t acc0) {
-  asm volatile(
-      "{\n\t.reg .pred p0, pt;\n\t.reg .b64 ra, rb;\n\t"
-      "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
-      "mov.b64 ra, %1;\n\tmov.b64 rb, %2;\n\t" PKV_MMA_SS("p0")
-      "add.s64 ra, %1, 2;\n\tadd.s64 rb, %2, 128;\n\t" PKV_MMA_SS("pt")
-      "add.s64 ra, %1, 4;\n\tadd.s64 rb, %2, 256;\n\t" PKV_MMA_SS("pt")
-      "add.s64 ra, %1, 6;\n\tadd.s64 rb, %2, 384;\n\t" PKV_MMA_SS("pt")
-      "add.s64 ra, %1, 1024;\n\tadd.s64 rb, %2, 512;\n\t" PKV_MMA_SS("pt")
-      "add.s64 ra, %1, 1026;\n\tadd.s64 rb, %2, 640;\n\t" PKV_MMA_SS("pt")
-      "add.s64 ra, %1, 1028;\n\tadd.s64 rb, %2, 768;\n\t" PKV_MMA_SS("pt")
-      "add.s64 ra, %1, 1030;\n\tadd.s64 rb, %2, 896;\n\t" PKV_MMA_SS("pt")
-      "}"
-      ::"r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "r"(acc0));
 }
 #define PKV_MMA_TS(acc) \
   "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %3, " acc ";\n\t"
@@ -255,6 +243,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
 // Bounded wait shared by all roles; the result is uniform across the warp.
 // Gives up when another role raised the abort flag or after kWaitLimitNs.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
@@ -276,65 +273,271 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded wait (one thread) until a counter in global memory reaches target;
+// gpu-scope acquire, so what was written before the count is visible after.
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target,
+                                           volatile uint32_t* abort) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1u;
+      atomicOr(&g_err_prefill, kErrTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// ------------------------------------------------------------------
+// Work decomposition (persistent CTAs, "stream-K" style).
+//
+// A unit is (sequence b, pair p of 128-row query tiles, query head hq); its
+// key blocks j = 0 .. nblk-1 cost one tile-block per tile that needs the
+// block (tile A needs blocks 0 .. nblk_a-1, tile B 0 .. nblk_b-1; nblk_b is
+// nblk_a or nblk_a + 1, or 0 when the pair's second tile is past the chunk).
+// Units are ordered by sequence, pairs from the last (heaviest) down, heads
+// innermost (the query heads of a KV head are neighbours, so they share K/V
+// through L2).  The total cost W is cut into Pe equal ranges, one per active
+// CTA (Pe = the grid, or fewer so that each range holds at least kMinCost);
+// a block belongs to the CTA whose range holds the block's starting cost
+// position.  A CTA therefore runs a sequence of segments (unit, blocks j0 ..
+// j1-1).  A range is at least 2 long and the block starts of a unit are at
+// most 2 apart, so the CTAs holding parts of one unit are consecutive: cf ..
+// cf + nown - 1; and since kMinCost exceeds the largest gap between block
+// starts (kUnitCost0 + 2), every active CTA has work.  The first part sits at
+// the end of CTA cf's range and goes to its tail slot 2 cf + 1; every other
+// part opens its CTA k's range and goes to its head slot 2 k.
+
+struct PairGeom {
+  int q0, q_len, L, row0, rows_a, rows_b, pmin_a, nblk_a, nblk_b, nblk;
+  int nd;                       // blocks both tiles need (cost 2 each); the rest cost 1
+};
+
+__device__ __forceinline__ bool seq_valid(const pkv_host::PrefillLaunch& a, int q0, int q_len,
+                                          int L) {
+  return q0 >= 0 && q_len >= 0 && q0 <= a.total_q - q_len && L >= q_len &&
+         L <= a.max_pages * kPageSize;
+}
+
+__device__ __forceinline__ int n_pairs_of(int q_len) { return (q_len + 2 * BM - 1) / (2 * BM); }
+
+__device__ __forceinline__ PairGeom pair_geom(int q0, int q_len, int L, int p) {
+  PairGeom g;
+  g.q0 = q0;
+  g.q_len = q_len;
+  g.L = L;
+  g.row0 = p * 2 * BM;
+  g.rows_a = max(0, min(BM, q_len - g.row0));
+  g.rows_b = max(0, min(BM, q_len - g.row0 - BM));
+  g.pmin_a = L - q_len + g.row0;
+  g.nblk_a = g.rows_a > 0 ? (g.pmin_a + g.rows_a - 1) / BN + 1 : 0;
+  g.nblk_b = g.rows_b > 0 ? (g.pmin_a + BM + g.rows_b - 1) / BN + 1 : 0;
+  g.nblk = max(g.nblk_a, g.nblk_b);
+  g.nd = min(g.nblk_a, g.nblk_b);
+  return g;
+}
+
+__device__ __forceinline__ int unit_cost(const PairGeom& g) {
+  return kUnitCost0 + g.nblk_a + g.nblk_b;
+}
+// cost offset of block j within its unit (the unit's fixed cost comes first)
+__device__ __forceinline__ int block_off(const PairGeom& g, int j) {
+  return kUnitCost0 + (j <= g.nd ? 2 * j : 2 * g.nd + (j - g.nd));
+}
+// first block whose starting offset is >= off (nblk if none)
+__device__ __forceinline__ int first_block_at(const PairGeom& g, long long off) {
+  if (off <= kUnitCost0) return 0;
+  off -= kUnitCost0;
+  const long long j = off <= 2 * g.nd ? (off + 1) / 2 : g.nd + (off - 2 * g.nd);
+  return j < g.nblk ? (int)j : g.nblk;
+}
+
+__device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, int b) {
+  const int q0 = a.cu_q[b];
+  const int q_len = a.cu_q[b + 1] - q0;
+  const int L = a.seq_lens[b];
+  if (!seq_valid(a, q0, q_len, L)) {
+    atomicOr(&g_err_prefill, kErrBadIndex);
+    return 0;
+  }
+  long long c = 0;
+  for (int p = 0; p < n_pairs_of(q_len); ++p) c += unit_cost(pair_geom(q0, q_len, L, p));
+  return c * a.num_q_heads;
+}
+
+// Position of the work walk: unit (b, pair index pi, head hq) and block j.
+struct Cursor {
+  int b, pi, hq, j;
+  long long ustart;             // cost position of the unit's first block
+  PairGeom g;
+  bool end;
+};
+
+__device__ __forceinline__ int pair_of(const Cursor& c) { return n_pairs_of(c.g.q_len) - 1 - c.pi; }
+
+// Total cost W, by one warp (every lane gets it).
+__device__ __forceinline__ long long total_cost(const pkv_host::PrefillLaunch& a, int lane) {
+  long long t = 0;
+  for (int b = lane; b < a.batch; b += 32) t += seq_cost(a, b);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
+}
+
+// The next unit (block 0) after the cursor's unit.
+__device__ __forceinline__ void next_unit(const pkv_host::PrefillLaunch& a, Cursor& c) {
+  c.ustart += unit_cost(c.g);
+  c.j = 0;
+  if (c.hq + 1 < a.num_q_heads) {
+    ++c.hq;
+    return;
+  }
+  c.hq = 0;
+  if (c.pi + 1 < n_pairs_of(c.g.q_len)) {
+    ++c.pi;
+    c.g = pair_geom(c.g.q0, c.g.q_len, c.g.L, pair_of(c));
+    return;
+  }
+  for (int b = c.b + 1; b < a.batch; ++b) {
+    const int q0 = a.cu_q[b], q_len = a.cu_q[b + 1] - q0, L = a.seq_lens[b];
+    if (!seq_valid(a, q0, q_len, L) || q_len == 0) continue;
+    c.b = b;
+    c.pi = 0;
+    c.g = pair_geom(q0, q_len, L, n_pairs_of(q_len) - 1);
+    return;
+  }
+  c.end = true;
+}
+
+// Cursor at the first block that starts at or after pos (0 <= pos < W), by
+// one warp (every lane gets the same cursor).
+__device__ __forceinline__ Cursor locate(const pkv_host::PrefillLaunch& a, long long pos, int lane) {
+  Cursor c;
+  c.end = true;
+  c.b = c.pi = c.hq = c.j = 0;
+  c.ustart = 0;
+  long long base = 0;
+  int bf = -1;
+  long long sb = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += 32) {
+    const int b = b0 + lane;
+    const long long cst = b < a.batch ? seq_cost(a, b) : 0;
+    long long incl = cst;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const long long excl = incl - cst;
+    const unsigned hit = __ballot_sync(0xffffffffu, b < a.batch && cst > 0 && base + incl > pos);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      bf = b0 + src;
+      sb = base + __shfl_sync(0xffffffffu, excl, src);
+      break;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (bf < 0) return c;
+  const int q0 = a.cu_q[bf], q_len = a.cu_q[bf + 1] - q0, L = a.seq_lens[bf];
+  long long p0 = sb;
+  const int np = n_pairs_of(q_len);
+  for (int pi = 0; pi < np; ++pi) {
+    const PairGeom g = pair_geom(q0, q_len, L, np - 1 - pi);
+    const long long cbp = (long long)unit_cost(g) * a.num_q_heads;
+    if (pos < p0 + cbp) {
+      const long long rel = pos < p0 ? 0 : pos - p0;
+      c.b = bf;
+      c.pi = pi;
+      c.hq = (int)(rel / unit_cost(g));
+      c.ustart = p0 + (long long)c.hq * unit_cost(g);
+      c.g = g;
+      c.j = first_block_at(g, pos - c.ustart);
+      c.end = false;
+      break;
+    }
+    p0 += cbp;
+  }
+  if (!c.end && c.j >= c.g.nblk) next_unit(a, c);
+  return c;
+}
+
+// Segment of the cursor's unit inside the cost range ending at hi: blocks
+// [c.j, returned j1).
+__device__ __forceinline__ int segment_end(const Cursor& c, long long hi) {
+  return first_block_at(c.g, hi - c.ustart);
+}
+
+__device__ __forceinline__ long long range_lo(long long W, int Pe, int k) { return W * k / Pe; }
+// the CTA whose range holds cost position pos
+__device__ __forceinline__ int owner_of(long long W, int Pe, long long pos) {
+  int k = (int)(pos * Pe / W);
+  while (k + 1 < Pe && range_lo(W, Pe, k + 1) <= pos) ++k;
+  return k;
+}
+__device__ __forceinline__ int active_ctas(long long W, int P) {
+  const long long n = W / kMinCost;
+  return (int)(n < 1 ? 1 : (n < P ? n : P));
+}
+
+// One segment as the producer publishes it to the other roles.
+struct SegDesc {
+  int qrow0;                    // q row of the unit's tile-A row 0
+  int hq, L, pmin_a, rows_a, rows_b, nblk_a, nblk_b;
+  int j0, j1;                   // blocks of this segment
+  int cf, nown;                 // CTAs holding parts of the unit; nown == 1: all here
+  int end;                      // no further segment
+  int pad[3];
+};
+static_assert(sizeof(SegDesc) == 64, "descriptor slot size");
+
 struct PrefillParams {
   pkv_host::PrefillLaunch a;
-  int n_pairs;                  // pairs of 128-row tiles of the longest chunk
+  uint32_t* counters;           // [2][P][2] parts done, then parts stored, per (first CTA, tile)
+  float* ws_lse;                // [2P slots][2 tiles][128] log2-domain lse of a part
+  float4* ws_o;                 // [2P slots][2 tiles][32 channel quads][128 rows] normalised O
 };
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                   const __grid_constant__ PrefillParams prm) {
+                   const __grid_constant__ CUtensorMap tq, const __grid_constant__ PrefillParams prm) {
   const pkv_host::PrefillLaunch& a = prm.a;
-  const int hq = blockIdx.x;
-  const int pair = prm.n_pairs - 1 - (int)blockIdx.y;   // heaviest tiles first
-  const int b = blockIdx.z;
   const int Hq = a.num_q_heads;
   const int G = Hq / a.num_kv_heads;
-  const int hkv = hq / G;
-
-  const int q0 = a.cu_q[b];
-  const int q_len = a.cu_q[b + 1] - q0;
-  if (q_len > prm.n_pairs * 2 * BM && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-    atomicOr(&g_err_prefill, kErrBadIndex);             // chunk longer than max_q_len
-  const int row0 = pair * 2 * BM;                       // first chunk row of tile A
-  if (row0 >= q_len) return;                            // no rows in this pair
-  const int L = a.seq_lens[b];
-  if (L < q_len || L > a.max_pages * kPageSize) {
-    if (threadIdx.x == 0) atomicOr(&g_err_prefill, kErrBadIndex);
-    return;
-  }
-  // tile x (0 = A, 1 = B): rows row0 + x*128 .. ; positions L - q_len + row
-  auto rows_of = [&](int x) { return max(0, min(BM, q_len - row0 - x * BM)); };
-  auto pmin_of = [&](int x) { return L - q_len + row0 + x * BM; };
-  auto nblk_of = [&](int x) {
-    const int rws = rows_of(x);
-    return rws > 0 ? (pmin_of(x) + rws - 1) / BN + 1 : 0;
-  };
-  const int nblk_a = nblk_of(0), nblk_b = nblk_of(1);
-  const int n_blk = max(nblk_a, nblk_b);
-  const int npages = (L + kPageSize - 1) / kPageSize;
+  const int P = gridDim.x, cta = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   const uint32_t base_s = (raw_s + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_s - raw_s);
   auto bar = [&](int i) -> uint32_t { return base_s + OFF_BAR + 8 * i; };
+  SegDesc* seg_ring = reinterpret_cast<SegDesc*>(base + OFF_SEG);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base + OFF_MISC + 4);
+  volatile uint32_t* merge_flag = reinterpret_cast<volatile uint32_t*>(base + OFF_MISC + 8);  // [2]
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(bar(BAR_Q), 2 * BM);
-    for (int s = 0; s < NSTAGE; ++s) {
-      mbar_init(bar(BAR_KF + s), 1);
-      mbar_init(bar(BAR_KE + s), 1);
-      mbar_init(bar(BAR_VF + s), 1);
-      mbar_init(bar(BAR_VE + s), 1);
-    }
     for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(BAR_QF + x), 1);
+      mbar_init(bar(BAR_QE + x), 1);
+      mbar_init(bar(BAR_KF + x), 1);
+      mbar_init(bar(BAR_KE + x), 1);
+      mbar_init(bar(BAR_VF + x), 1);
+      mbar_init(bar(BAR_VE + x), 1);
       mbar_init(bar(BAR_SF + x), 1);
       mbar_init(bar(BAR_PF + x), BM);
       mbar_init(bar(BAR_OD + x), 1);
+      mbar_init(bar(BAR_SEGF + x), 1);
+      mbar_init(bar(BAR_SEGE + x), 9);            // 8 softmax warps + the MMA warp
+      mbar_init(bar(BAR_EPI + x), 4);             // the tile's 4 softmax warps
+      mbar_init(bar(BAR_MRG + x), 1);
+      mbar_init(bar(BAR_ST + x), 4);
+      mbar_init(bar(BAR_GO + x), 1);
     }
     mbar_init(bar(BAR_DR), 1);
     *abort_flag = 0u;
@@ -351,115 +554,220 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   static_assert(NSTAGE == 2, "the producer tracks two stages");
-  int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1;   // last block issued per stage
+  // last issued load per K/V stage and number of Q loads per tile (for the
+  // drain after an abort)
+  int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1, nq_a = 0, nq_b = 0;
   if (warp == WARP_TMA) {
-    // ------------------------------------------------------ TMA producer
-    const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
+    // ------------------------------------------------ scheduler + producer
+    const long long W = total_cost(a, lane);
+    const int Pe = active_ctas(W, P);
+    long long lo = 0, hi = 0;
+    if (cta < Pe) {
+      lo = range_lo(W, Pe, cta);
+      hi = range_lo(W, Pe, cta + 1);
+    }
+    Cursor c;
+    c.end = true;
+    if (lo < hi) c = locate(a, lo, lane);
     bool ok = true;
-    for (int j = 0; j < n_blk && ok; ++j) {
-      const int st = j % NSTAGE;
-      const int lp = j * (BN / kPageSize) + (lane & 7);
-      int pg = 0;
-      if (lane < 8 && lp < npages) {
-        pg = __ldg(bt_row + lp);
+    int t = 0;                                    // K/V blocks issued so far
+    for (int sg = 0;; ++sg) {
+      const bool has = !c.end && c.ustart + block_off(c.g, c.j) < hi;
+      const int ri = sg % NSEG;
+      if (sg >= NSEG && !(ok = wait_bar(bar(BAR_SEGE + ri), ((sg / NSEG) - 1) & 1, abort_flag)))
+        break;
+      const int j0 = c.j, j1 = has ? segment_end(c, hi) : 0;
+      if (lane == 0) {
+        SegDesc& d = seg_ring[ri];
+        d.end = has ? 0 : 1;
+        if (has) {
+          d.qrow0 = c.g.q0 + c.g.row0;
+          d.hq = c.hq;
+          d.L = c.g.L;
+          d.pmin_a = c.g.pmin_a;
+          d.rows_a = c.g.rows_a;
+          d.rows_b = c.g.rows_b;
+          d.nblk_a = c.g.nblk_a;
+          d.nblk_b = c.g.nblk_b;
+          d.j0 = j0;
+          d.j1 = j1;
+          const int cf = owner_of(W, Pe, c.ustart + block_off(c.g, 0));
+          d.cf = cf;
+          d.nown = owner_of(W, Pe, c.ustart + block_off(c.g, c.g.nblk - 1)) - cf + 1;
+        }
+        mbar_arrive(bar(BAR_SEGF + ri));          // release: the fields above are visible
+      }
+      __syncwarp();
+      if (!has) break;
+
+      const int hkv = c.hq / G;
+      const int npages = (c.g.L + kPageSize - 1) / kPageSize;
+      const int32_t* bt_row = a.block_table + (size_t)c.b * a.max_pages;
+      // Page ids of block j, one per lane 0..7 (0 past the sequence's pages).
+      auto page_ids = [&](int j) -> int {
+        const int lp = j * (BN / kPageSize) + lane;
+        return (lane < BN / kPageSize && lp < npages) ? __ldg(bt_row + lp) : 0;
+      };
+      // K and V of block j (global block index t): the K boxes, then (after
+      // `between`) the V boxes.  Lane i < 8 loads page i of the block (both
+      // 64-channel halves), so a block takes four TMA instructions, and the
+      // next block's page ids are read while this block's waits run.
+      int pg_next = page_ids(j0);
+      auto issue_kv = [&](int j, auto&& between) -> bool {
+        const int st = t % NSTAGE;
+        int pg = pg_next;
+        if (j + 1 < j1) pg_next = page_ids(j + 1);
         if (pg < 0 || pg >= a.num_pages) {
           atomicOr(&g_err_prefill, kErrBadIndex);
           pg = 0;
         }
-      }
-      // lanes 0..7 hold the block's page ids; lane 0 needs them all
-      int rowk[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        rowk[i] = (__shfl_sync(0xffffffffu, pg, i) * a.num_kv_heads + hkv) * kPageSize;
-      const int nload = min(BN / kPageSize, npages - j * (BN / kPageSize));
-      const uint32_t bytes = (uint32_t)nload * 2u * (kPageSize * 64 * 2);
-      if (j >= NSTAGE && !(ok = wait_bar(bar(BAR_KE + st), ((j / NSTAGE) - 1) & 1, abort_flag)))
-        break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(BAR_KF + st), bytes);
-        const uint32_t dst = base_s + OFF_K + st * TILE;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (i < nload) {
-            tma_load_2d(dst + i * 2048, &tk, 0, rowk[i], bar(BAR_KF + st));
-            tma_load_2d(dst + HALF + i * 2048, &tk, 64, rowk[i], bar(BAR_KF + st));
-          }
+        const int rowk = (pg * a.num_kv_heads + hkv) * kPageSize;
+        const int nload = min(BN / kPageSize, npages - j * (BN / kPageSize));
+        const uint32_t bytes = (uint32_t)nload * 2u * (kPageSize * 64 * 2);
+        if (t >= NSTAGE && !wait_bar(bar(BAR_KE + st), ((t / NSTAGE) - 1) & 1, abort_flag))
+          return false;
+        if (lane == 0) mbar_arrive_expect_tx(bar(BAR_KF + st), bytes);
+        __syncwarp();
+        if (lane < nload) {
+          const uint32_t dst = base_s + OFF_K + st * TILE + lane * 2048;
+          tma_load_2d(dst, &tk, 0, rowk, bar(BAR_KF + st));
+          tma_load_2d(dst + HALF, &tk, 64, rowk, bar(BAR_KF + st));
         }
-      }
-      (st == 0 ? last_k0 : last_k1) = j;
-      if (j >= NSTAGE && !(ok = wait_bar(bar(BAR_VE + st), ((j / NSTAGE) - 1) & 1, abort_flag)))
-        break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bar(BAR_VF + st), bytes);
-        const uint32_t dst = base_s + OFF_V + st * TILE;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (i < nload) {
-            tma_load_2d(dst + i * 2048, &tv, 0, rowk[i], bar(BAR_VF + st));
-            tma_load_2d(dst + HALF + i * 2048, &tv, 64, rowk[i], bar(BAR_VF + st));
-          }
+        (st == 0 ? last_k0 : last_k1) = t;
+        if (!between()) return false;
+        if (t >= NSTAGE && !wait_bar(bar(BAR_VE + st), ((t / NSTAGE) - 1) & 1, abort_flag))
+          return false;
+        if (lane == 0) mbar_arrive_expect_tx(bar(BAR_VF + st), bytes);
+        __syncwarp();
+        if (lane < nload) {
+          const uint32_t dst = base_s + OFF_V + st * TILE + lane * 2048;
+          tma_load_2d(dst, &tv, 0, rowk, bar(BAR_VF + st));
+          tma_load_2d(dst + HALF, &tv, 64, rowk, bar(BAR_VF + st));
         }
-      }
-      (st == 0 ? last_v0 : last_v1) = j;
+        (st == 0 ? last_v0 : last_v1) = t;
+        ++t;
+        return true;
+      };
+      // The segment's Q tiles, each once the previous segment's last QK of
+      // that tile has completed.  They go between the first block's K (whose
+      // stage frees early) and its V (whose stage frees only when the
+      // previous segment's second-to-last PV is done), so that they land
+      // while the previous segment is still finishing.
+      auto issue_q = [&]() -> bool {
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (sg > 0 && !wait_bar(bar(BAR_QE + x), (sg - 1) & 1, abort_flag)) return false;
+          const int rows = x == 0 ? c.g.rows_a : c.g.rows_b;
+          if (lane == 0) {
+            if (rows > 0) {
+              // rows past the end of q read as zeros; rows of the next
+              // sequence only feed padding rows, whose results are never stored
+              const int row = c.g.q0 + c.g.row0 + x * BM;
+              const uint32_t dst = base_s + OFF_Q + x * TILE;
+              mbar_arrive_expect_tx(bar(BAR_QF + x), (uint32_t)TILE);
+              tma_load_3d(dst, &tq, 0, c.hq, row, bar(BAR_QF + x));
+              tma_load_3d(dst + HALF, &tq, 64, c.hq, row, bar(BAR_QF + x));
+            } else {
+              mbar_arrive(bar(BAR_QF + x));
+            }
+          }
+          (x == 0 ? nq_a : nq_b) = sg + 1;
+        }
+        return true;
+      };
+      auto nothing = []() { return true; };
+
+      if (!(ok = issue_kv(j0, issue_q))) break;
+      for (int j = j0 + 1; j < j1; ++j)
+        if (!(ok = issue_kv(j, nothing))) break;
+      if (!ok) break;
+      next_unit(a, c);
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------- MMA issuer
-    // Iteration j: PV_A(j-1), QK_A(j), PV_B(j-1), QK_B(j).  While softmax A
-    // works on S_A(j) the tensor core runs PV_B(j-1) and QK_B(j), and the
-    // other way round.  QK_x(j) overwrites S_x, which holds P_x(j-1): it is
-    // issued after PV_x(j-1), and MMAs of one thread run in issue order.
-    bool ok = wait_bar(bar(BAR_Q), 0, abort_flag);
-    for (int j = 0; j <= n_blk && ok; ++j) {
-      const bool has_qk = j < n_blk;
-      const int st = j % NSTAGE, pst = (j + NSTAGE - 1) % NSTAGE;
-      if (has_qk && !(ok = wait_bar(bar(BAR_KF + st), (j / NSTAGE) & 1, abort_flag))) break;
-      if (j >= 1) {
-        if (!(ok = wait_bar(bar(BAR_VF + pst), ((j - 1) / NSTAGE) & 1, abort_flag))) break;
-        const int kbase = (j - 1) * BN;
-        if (kbase + BN > L) {
-          // zero V rows at positions >= L (both 64-channel halves of each row)
-          const int first = L - kbase;
-          uint8_t* vt = base + OFF_V + pst * TILE;
-          for (int idx = lane; idx < (BN - first) * 16; idx += 32) {
-            const int row = first + (idx >> 4), c = idx & 15;
-            *reinterpret_cast<uint4*>(vt + (c >> 3) * HALF + row * 128 + (c & 7) * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_async_smem();
-          __syncwarp();
-        }
-      }
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        const int nbx = x == 0 ? nblk_a : nblk_b;
-        if (j >= 1 && j - 1 < nbx) {
-          if (!(ok = wait_bar(bar(BAR_PF + x), (j - 1) & 1, abort_flag))) break;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t v_s = base_s + OFF_V + pst * TILE;
-            mma8_pv_ts(tmem + tm_o(x), tmem + tm_p(x), desc_mnmajor(v_s), IDESC_PV,
-                       j > 1 ? 1u : 0u);
-            if (j - 1 == nbx - 1) mma_commit(bar(BAR_OD + x));
-          }
-          __syncwarp();
-        }
-        if (has_qk && j < nbx) {
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t q_s = base_s + OFF_Q + x * TILE, k_s = base_s + OFF_K + st * TILE;
-            mma8_qk(tmem + tm_s(x), desc_kmajor(q_s), desc_kmajor(k_s), IDESC_QK);
-            mma_commit(bar(BAR_SF + x));
-          }
-          __syncwarp();
-        }
-      }
-      if (!ok) break;
+    // Per segment, iteration j issues PV_A(j-1), QK_A(j), PV_B(j-1), QK_B(j).
+    // While softmax A works on S_A(j) the tensor core runs PV_B(j-1) and
+    // QK_B(j), and the other way round.  QK_x(j) overwrites S_x, which holds
+    // P_x(j-1): it is issued after PV_x(j-1), and MMAs of one thread run in
+    // issue order.  A segment's first QKs only touch S, so they overlap the
+    // previous segment's epilogue, which reads O.
+    bool ok = true;
+    int t = 0, cnt_a = 0, cnt_b = 0;
+    for (int sg = 0;; ++sg) {
+      const int ri = sg % NSEG;
+      if (!(ok = wait_bar(bar(BAR_SEGF + ri), (sg / NSEG) & 1, abort_flag))) break;
+      const SegDesc& d = seg_ring[ri];
+      const int end = d.end;
+      const int j0 = d.j0, j1 = d.j1, L = d.L;
+      const int je_a = min(j1, d.nblk_a), je_b = min(j1, d.nblk_b);
+      __syncwarp();
+      if (end) break;
+      if (lane == 0) mbar_arrive(bar(BAR_SEGE + ri));
+      if (!(ok = wait_bar(bar(BAR_QF + 0), sg & 1, abort_flag))) break;
+      if (!(ok = wait_bar(bar(BAR_QF + 1), sg & 1, abort_flag))) break;
       if (lane == 0) {
-        if (has_qk) mma_commit(bar(BAR_KE + st));
-        if (j >= 1) mma_commit(bar(BAR_VE + pst));
+        // a tile without QK in this segment releases its Q at once
+        if (je_a <= j0) mma_commit(bar(BAR_QE + 0));
+        if (je_b <= j0) mma_commit(bar(BAR_QE + 1));
       }
       __syncwarp();
+      for (int j = j0; j <= j1 && ok; ++j) {
+        const bool has_qk = j < j1;
+        const int tt = t + (j - j0);              // global block index of block j
+        const int st = tt % NSTAGE, pst = (tt + NSTAGE - 1) % NSTAGE;
+        if (has_qk && !(ok = wait_bar(bar(BAR_KF + st), (tt / NSTAGE) & 1, abort_flag))) break;
+        if (j > j0) {
+          if (!(ok = wait_bar(bar(BAR_VF + pst), ((tt - 1) / NSTAGE) & 1, abort_flag))) break;
+          const int kbase = (j - 1) * BN;
+          if (kbase + BN > L) {
+            // zero V rows at positions >= L (both 64-channel halves of each row)
+            const int first_row = L - kbase;
+            uint8_t* vt = base + OFF_V + pst * TILE;
+            for (int idx = lane; idx < (BN - first_row) * 16; idx += 32) {
+              const int row = first_row + (idx >> 4), cc = idx & 15;
+              *reinterpret_cast<uint4*>(vt + (cc >> 3) * HALF + row * 128 + (cc & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_async_smem();
+            __syncwarp();
+          }
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          const int jex = x == 0 ? je_a : je_b;
+          int& cnt = x == 0 ? cnt_a : cnt_b;
+          if (j > j0 && j - 1 < jex) {
+            if (!(ok = wait_bar(bar(BAR_PF + x), cnt & 1, abort_flag))) break;
+            ++cnt;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t v_s = base_s + OFF_V + pst * TILE;
+              mma8_pv_ts(tmem + tm_o(x), tmem + tm_p(x), desc_mnmajor(v_s), IDESC_PV,
+                         j - 1 > j0 ? 1u : 0u);
+              if (j == jex) mma_commit(bar(BAR_OD + x));
+            }
+            __syncwarp();
+          }
+          if (has_qk && j < jex) {
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t q_s = base_s + OFF_Q + x * TILE, k_s = base_s + OFF_K + st * TILE;
+              mma8_qk(tmem + tm_s(x), desc_kmajor(q_s), desc_kmajor(k_s), IDESC_QK);
+              mma_commit(bar(BAR_SF + x));
+              if (j == jex - 1) mma_commit(bar(BAR_QE + x));
+            }
+            __syncwarp();
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (has_qk) mma_commit(bar(BAR_KE + st));
+          if (j > j0) mma_commit(bar(BAR_VE + pst));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      t += j1 - j0;
     }
     // drain: every MMA issued above completes before TMEM is released
     if (lane == 0) mma_commit(bar(BAR_DR));
@@ -467,128 +775,275 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     (void)mbar_wait(bar(BAR_DR), 0);
   } else {
     // ---------------------------------------------------------- softmax
+    // Per segment the block loop keeps only what it needs in registers; the
+    // rest is read again from the segment's descriptor afterwards (it stays
+    // valid until this warp releases it at the end of the segment).
     const int x = warp >> 2;                      // tile: 0 = A, 1 = B
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;            // row of the tile
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int rows = rows_of(x);
-    const int pos_min = pmin_of(x);
-    const int n_x = x == 0 ? nblk_a : nblk_b;
-    const int pos_r = min(pos_min + r, L - 1);    // padding rows clamp to the last key
-    const bool row_valid = r < rows;
-    const int qrow0 = q0 + row0 + x * BM;         // chunk row of tile row 0
-
-    // Q tile -> swizzled shared memory (rows past the chunk are zero).
-    {
-      const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
-      uint8_t* qs = base + OFF_Q + x * TILE;
-      for (int it = 0; it < 16; ++it) {
-        const int row = quarter * 32 + 2 * it + (lane >> 4);
-        const int c = lane & 15;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row < rows)
-          v = __ldg(reinterpret_cast<const uint4*>(
-                        qg + ((size_t)(qrow0 + row) * Hq + hq) * kHeadDim) + c);
-        *reinterpret_cast<uint4*>(qs + (c >> 3) * HALF + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
-            v;
-      }
-      fence_async_smem();
-      mbar_arrive(bar(BAR_Q));
-    }
-
     const float sl2 = a.softmax_scale * kLog2e;
     const float2 sl2x2 = make_float2(sl2, sl2);
-    float m_run = -INFINITY, l_run = 0.f;        // running max (scaled, log2 domain), sum
     bool ok = true;
-    for (int j = 0; j < n_x; ++j) {
-      if (!(ok = wait_bar(bar(BAR_SF + x), j & 1, abort_flag))) break;
-      tc_fence_after();
-      // The whole S row in one round trip (two 64-column loads, one wait);
-      // packed P then overwrites the S registers it came from (c <= 2c) and
-      // goes to TMEM columns 64..127 of S_x, which are consumed by then.
-      const int kbase = j * BN;
-      uint32_t sr[128];
-      tmem_ld64(t_lane + tm_s(x), *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
-      tmem_ld64(t_lane + tm_s(x) + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
-      tmem_wait_ld();
-      if (kbase + BN - 1 > pos_min) {             // block crosses the causal edge
-        const int lim = pos_r - kbase;
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+    // phase parities: s_full, o_done, epi/mrg, st, go
+    constexpr uint32_t PAR_S = 1, PAR_O = 2, PAR_C = 4, PAR_ST = 8, PAR_GO = 16;
+    uint32_t par = 0;
+    for (int sg = 0;; ++sg) {
+      const int ri = sg % NSEG;
+      if (!(ok = wait_bar(bar(BAR_SEGF + ri), (sg / NSEG) & 1, abort_flag))) break;
+      volatile const SegDesc* d = seg_ring + ri;
+      auto release = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_SEGE + ri));
+      };
+      if (d->end) break;
+      if ((x == 0 ? d->rows_a : d->rows_b) == 0) {   // second tile past the chunk: no work
+        release();
+        continue;
       }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < BN; c += 2)
-        mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sr[c]),
-                                 __uint_as_float(sr[c + 1]));
-      const float m_blk = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
-      const float m_new = fmaxf(m_run, m_blk);
-      const bool need = m_new > m_run + 8.0f;     // lazy rescale threshold (2^8)
-      const float m_use = need ? m_new : m_run;
-      const float alpha = need ? fast_exp2(m_run - m_use) : 1.0f;
-      const float2 negm = make_float2(-m_use, -m_use);
-      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < BN / 2; ++c) {
-        const float2 t = fma2(make_float2(__uint_as_float(sr[2 * c]),
-                                          __uint_as_float(sr[2 * c + 1])), sl2x2, negm);
-        const float2 pp = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-        sum2[c & 1] = add2(sum2[c & 1], pp);
-        sr[c] = pack_bf16x2(pp.x, pp.y);
-      }
-      tmem_st64(t_lane + tm_p(x), *reinterpret_cast<const uint32_t(*)[64]>(&sr[0]));
-      const float2 s2 = add2(sum2[0], sum2[1]);
-      l_run = l_run * alpha + (s2.x + s2.y);
-      m_run = m_use;
+      const int j0 = d->j0;
+      const int jend = min(d->j1, x == 0 ? d->nblk_a : d->nblk_b);
+      const int pos_min = d->pmin_a + x * BM;
+      const int pos_r = min(pos_min + r, d->L - 1);   // padding rows clamp to the last key
 
-      // O rescale: S_x(j) complete implies PV_x(j-1) complete (one thread
-      // issues both, in order), so O_x is stable here.
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        const float2 a2 = make_float2(alpha, alpha);
+      // Running max (scaled, log2 domain) and sum.  The max starts finite and
+      // far below any score: a row with no unmasked key yet (only when a
+      // segment starts past block 0) then gets P = 2^(-inf + 1e30) = 0
+      // instead of 2^(-inf + inf) = NaN, and its first real block rescales
+      // by 2^(-1e30 - m) = 0.
+      float m_run = -1e30f, l_run = 0.f;
+      for (int j = j0; j < jend; ++j) {
+        if (!(ok = wait_bar(bar(BAR_SF + x), par & PAR_S, abort_flag))) break;
+        par ^= PAR_S;
+        tc_fence_after();
+        // The whole S row in one round trip; packed P then overwrites the S
+        // registers it came from (c <= 2c) and goes to TMEM columns 64..127
+        // of S_x, which are consumed by then.
+        const int kbase = j * BN;
+        uint32_t sr[128];
+        tmem_ld64(t_lane + tm_s(x), *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
+        tmem_ld64(t_lane + tm_s(x) + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
+        tmem_wait_ld();
+        if (kbase + BN - 1 > pos_min) {           // block crosses the causal edge
+          const int lim = pos_r - kbase;
+#pragma unroll
+          for (int cc = 0; cc < BN; ++cc)
+            if (cc > lim) sr[cc] = __float_as_uint(-INFINITY);
+        }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int cc = 0; cc < BN; cc += 2)
+          mx[(cc >> 1) & 3] = fmax3(mx[(cc >> 1) & 3], __uint_as_float(sr[cc]),
+                                    __uint_as_float(sr[cc + 1]));
+        const float m_blk = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;
+        const float m_new = fmaxf(m_run, m_blk);
+        const bool need = m_new > m_run + 8.0f;   // lazy rescale threshold (2^8)
+        const float m_use = need ? m_new : m_run;
+        const float alpha = need ? fast_exp2(m_run - m_use) : 1.0f;
+        const float2 negm = make_float2(-m_use, -m_use);
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int cc = 0; cc < BN / 2; ++cc) {
+          const float2 tv2 = fma2(make_float2(__uint_as_float(sr[2 * cc]),
+                                              __uint_as_float(sr[2 * cc + 1])), sl2x2, negm);
+          const float2 pp = make_float2(fast_exp2(tv2.x), fast_exp2(tv2.y));
+          sum2[cc & 1] = add2(sum2[cc & 1], pp);
+          sr[cc] = pack_bf16x2(pp.x, pp.y);
+        }
+        tmem_st64(t_lane + tm_p(x), *reinterpret_cast<const uint32_t(*)[64]>(&sr[0]));
+        const float2 s2 = add2(sum2[0], sum2[1]);
+        l_run = l_run * alpha + (s2.x + s2.y);
+        m_run = m_use;
+
+        // O rescale: S_x(j) complete implies PV_x(j-1) complete (one thread
+        // issues both, in order), so O_x is stable here.
+        if (j > j0 && __any_sync(0xffffffffu, need)) {
+          const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+          for (int h = 0; h < 4; ++h) {
+            uint32_t o[32];
+            tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
+              o[i] = __float_as_uint(v.x);
+              o[i + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(t_lane + tm_o(x) + 32 * h, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(BAR_PF + x));
+      }
+      if (!ok) break;
+      const bool own = jend > j0;                 // this segment saw keys of this tile
+      if (own) {
+        if (!(ok = wait_bar(bar(BAR_OD + x), (par & PAR_O) ? 1u : 0u, abort_flag))) break;
+        par ^= PAR_O;
+        tc_fence_after();
+      }
+      const int qrow0 = d->qrow0 + x * BM;        // q row of this tile's row 0
+      const int hq = d->hq;
+      const int nown = d->nown;
+      const bool row_valid = r < (x == 0 ? d->rows_a : d->rows_b);
+      const float inv = 1.0f / l_run;
+      if (nown == 1) {
+        // ---- the whole unit ran here: normalise and store
+        const size_t orow = ((size_t)(qrow0 + r) * Hq + hq) * kHeadDim;
+        uint4* og = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
 #pragma unroll 1
         for (int h = 0; h < 4; ++h) {
           uint32_t o[32];
           tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
           tmem_wait_ld();
+          if (row_valid) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 v = mul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2);
-            o[i] = __float_as_uint(v.x);
-            o[i + 1] = __float_as_uint(v.y);
+            for (int k = 0; k < 4; ++k) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
+              v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
+              v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
+              v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+              og[4 * h + k] = v;
+            }
           }
-          tmem_st32(t_lane + tm_o(x) + 32 * h, o);
+        }
+        if (row_valid && a.lse)
+          a.lse[(size_t)(qrow0 + r) * Hq + hq] = (m_run + fast_log2(l_run)) * kLn2;
+        release();
+        continue;
+      }
+
+      // ---- one part of a unit cut between CTAs.  The part is counted first;
+      // the last part to be counted merges all of them (its own straight from
+      // TMEM), every other part is stored to the workspace and then counted
+      // as stored, which the merging CTA waits for (those CTAs are running:
+      // they have counted their part, and storing it needs nothing else).
+      const int cf = d->cf;
+      uint32_t* ctr_done = prm.counters + 2 * cf + x;
+      uint32_t* ctr_stored = prm.counters + 2 * P + 2 * cf + x;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_EPI + x));
+      if (quarter == 0) {
+        if (!(ok = wait_bar(bar(BAR_EPI + x), (par & PAR_C) ? 1u : 0u, abort_flag))) break;
+        if (lane == 0) {
+          merge_flag[x] = atomicAdd(ctr_done, 1u) == (uint32_t)(nown - 1) ? 1u : 0u;
+          mbar_arrive(bar(BAR_MRG + x));
         }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(BAR_PF + x));
-    }
-
-    if (ok && n_x > 0 && wait_bar(bar(BAR_OD + x), 0, abort_flag)) {
-      tc_fence_after();
-      const float inv = 1.0f / l_run;
+      if (!(ok = wait_bar(bar(BAR_MRG + x), (par & PAR_C) ? 1u : 0u, abort_flag))) break;
+      par ^= PAR_C;
+      if (!merge_flag[x]) {
+        const size_t prow = (size_t)((2 * cta + (cta == cf ? 1 : 0)) * 2 + x);
+        if (own) {
+          float4* wo = prm.ws_o + prow * 32 * BM + r;
+#pragma unroll 1
+          for (int h = 0; h < 4; ++h) {
+            uint32_t o[32];
+            tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              wo[(8 * h + k) * BM] =
+                  make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                              __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+          }
+          prm.ws_lse[prow * BM + r] = m_run + fast_log2(l_run);
+        } else {
+          prm.ws_lse[prow * BM + r] = -INFINITY;  // no key of this tile in this part
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_ST + x));
+        if (quarter == 0) {
+          if (!(ok = wait_bar(bar(BAR_ST + x), (par & PAR_ST) ? 1u : 0u, abort_flag))) break;
+          if (lane == 0) {
+            __threadfence();
+            atomicAdd(ctr_stored, 1u);
+          }
+        }
+        par ^= PAR_ST;
+        release();
+        continue;
+      }
+      // the last part: wait until every other part is stored, then merge
+      if (quarter == 0 && lane == 0) {
+        if (wait_count(ctr_stored, (uint32_t)(nown - 1), abort_flag)) {
+          *ctr_done = 0u;                         // ready for the next call
+          *ctr_stored = 0u;
+          mbar_arrive(bar(BAR_GO + x));
+        }
+      }
+      __syncwarp();
+      if (!(ok = wait_bar(bar(BAR_GO + x), (par & PAR_GO) ? 1u : 0u, abort_flag))) break;
+      par ^= PAR_GO;
+      __threadfence();
+      // Parts of CTAs cf .. cf + nown - 1: cf's tail slot, the head slot of
+      // every later CTA, this CTA's own part from TMEM.  Every part enters as
+      // the stored parts do (O / l rounded to fp32, lse = m + log2 l), in CTA
+      // order, so the result does not depend on which CTA merges.
+      const float lse_own = own ? m_run + fast_log2(l_run) : -INFINITY;
+      auto part_lse = [&](int k) -> float {
+        if (k == cta) return lse_own;
+        const int sk = k == cf ? 2 * cf + 1 : 2 * k;
+        return __ldcg(prm.ws_lse + (size_t)(sk * 2 + x) * BM + r);
+      };
+      float M = -INFINITY;
+      for (int k = cf; k < cf + nown; ++k) M = fmaxf(M, part_lse(k));
+      float sum = 0.f;
       const size_t orow = ((size_t)(qrow0 + r) * Hq + hq) * kHeadDim;
       uint4* og = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
 #pragma unroll 1
-      for (int h = 0; h < 4; ++h) {
-        uint32_t o[32];
-        tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
-        tmem_wait_ld();
+      for (int h = 0; h < 4; ++h) {             // 32 channels at a time
+        float acc[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        for (int k = cf; k < cf + nown; ++k) {
+          const float ls = part_lse(k);
+          const float f = ls == -INFINITY ? 0.f : fast_exp2(ls - M);   // 0: no keys, no O
+          if (h == 0) sum += f;
+          if (k == cta) {
+            if (own) {                            // warp-uniform
+              uint32_t o[32];
+              tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
+              tmem_wait_ld();
+              if (f != 0.f) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc[i] = fmaf(f, __uint_as_float(o[i]) * inv, acc[i]);
+              }
+            }
+          } else if (f != 0.f) {
+            const size_t pk = (size_t)((k == cf ? 2 * cf + 1 : 2 * k) * 2 + x);
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(prm.ws_o + (pk * 32 + 8 * h + i) * BM + r);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              acc[4 * i + 0] = fmaf(f, v[i].x, acc[4 * i + 0]);
+              acc[4 * i + 1] = fmaf(f, v[i].y, acc[4 * i + 1]);
+              acc[4 * i + 2] = fmaf(f, v[i].z, acc[4 * i + 2]);
+              acc[4 * i + 3] = fmaf(f, v[i].w, acc[4 * i + 3]);
+            }
+          }
+        }
+        const float is = sum > 0.f ? 1.0f / sum : 0.f;
         if (row_valid) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
-            og[4 * h + k] = v;
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16x2(acc[8 * i + 0] * is, acc[8 * i + 1] * is);
+            w.y = pack_bf16x2(acc[8 * i + 2] * is, acc[8 * i + 3] * is);
+            w.z = pack_bf16x2(acc[8 * i + 4] * is, acc[8 * i + 5] * is);
+            w.w = pack_bf16x2(acc[8 * i + 6] * is, acc[8 * i + 7] * is);
+            og[4 * h + i] = w;
           }
         }
       }
       if (row_valid && a.lse)
-        a.lse[(size_t)(qrow0 + r) * Hq + hq] = (m_run + fast_log2(l_run)) * kLn2;
+        a.lse[(size_t)(qrow0 + r) * Hq + hq] = sum > 0.f ? (M + fast_log2(sum)) * kLn2 : -INFINITY;
+      release();
     }
   }
 
@@ -600,6 +1055,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (last_k1 >= 0) (void)mbar_wait(bar(BAR_KF + 1), (last_k1 / NSTAGE) & 1);
     if (last_v0 >= 0) (void)mbar_wait(bar(BAR_VF + 0), (last_v0 / NSTAGE) & 1);
     if (last_v1 >= 0) (void)mbar_wait(bar(BAR_VF + 1), (last_v1 / NSTAGE) & 1);
+    if (nq_a > 0) (void)mbar_wait(bar(BAR_QF + 0), (nq_a - 1) & 1);
+    if (nq_b > 0) (void)mbar_wait(bar(BAR_QF + 1), (nq_b - 1) & 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -643,6 +1100,25 @@ bool encode_pool_map(CUtensorMap* m, const void* base, int num_pages, int hkv) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q [total_q][Hq][128] as a 3-D bf16 tensor (channel, head, row); a box is
+// 64 channels of one head over 128 rows, 128B-swizzled: one half of a query
+// tile in the K-major layout the QK MMA reads.  Rows past total_q read as 0.
+bool encode_q_map(CUtensorMap* m, const void* q, int total_q, int hq) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hq, (cuuint64_t)total_q};
+  cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)hq * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)BM};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Workspace: per-(CTA, tile) part counters, then the parts' lse, then their O.
+size_t ws_counter_bytes(int ctas) { return ((size_t)4 * ctas * 4 + 255) / 256 * 256; }
+size_t ws_lse_bytes(int ctas) { return (size_t)2 * ctas * SLOT_ROWS * 4; }
+
 }  // namespace
 
 namespace pkv_host {
@@ -650,9 +1126,10 @@ namespace pkv_host {
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
   if ((long long)a.num_pages * a.num_kv_heads * kPageSize >= (1ll << 31))
     return cudaErrorNotSupported;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tq;
   if (!encode_pool_map(&tk, a.k, a.num_pages, a.num_kv_heads) ||
-      !encode_pool_map(&tv, a.v, a.num_pages, a.num_kv_heads))
+      !encode_pool_map(&tv, a.v, a.num_pages, a.num_kv_heads) ||
+      !encode_q_map(&tq, a.q, a.total_q, a.num_q_heads))
     return cudaErrorInvalidValue;
   static bool configured = false;
   if (!configured) {
@@ -661,11 +1138,22 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  PrefillParams prm{a, (a.max_q_len + 2 * BM - 1) / (2 * BM)};
-  dim3 grid(a.num_q_heads, prm.n_pairs, a.batch);
-  prefill_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tk, tv, prm);
+  if (a.ctas <= 0 || a.ctas > kMaxPrefillCtas || !a.workspace) return cudaErrorInvalidValue;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  PrefillParams prm{a, reinterpret_cast<uint32_t*>(ws),
+                    reinterpret_cast<float*>(ws + ws_counter_bytes(a.ctas)),
+                    reinterpret_cast<float4*>(ws + ws_counter_bytes(a.ctas) + ws_lse_bytes(a.ctas))};
+  prefill_kernel<<<a.ctas, NUM_THREADS, SMEM_BYTES, s>>>(tk, tv, tq, prm);
   return cudaGetLastError();
 }
+
+int prefill_ctas(int sms) { return sms < kMaxPrefillCtas ? sms : kMaxPrefillCtas; }
+
+size_t prefill_workspace_bytes(int ctas) {
+  return ws_counter_bytes(ctas) + ws_lse_bytes(ctas) + (size_t)2 * ctas * SLOT_ROWS * kHeadDim * 4;
+}
+
+size_t prefill_workspace_zero_bytes(int ctas) { return ws_counter_bytes(ctas); }
 
 uint32_t take_prefill_error(cudaStream_t s) {
   uint32_t h = 0, zero = 0;

@@ -49,7 +49,9 @@ SIGNATURES = {
                                    _P, _P, _P]),
     "pkv_paged_attn_decode_noalloc": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P,
                                            _P, _P]),
-    "pkv_paged_attn_prefill": (_I, [_POOLP, _P, _P, _I, _I, _P, _I, _P, _I, _F, _P, _P, _P]),
+    "pkv_prefill_plan": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
+    "pkv_paged_attn_prefill": (_I, [_POOLP, _P, _I, _P, _I, _I, _P, _I, _P, _I, _F, _P, _SZ, _P,
+                                    _P, _P]),
     "pkv_poll_device_error": (_I, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
     "pkv_device_sm_count": (_I, []),
@@ -210,22 +212,44 @@ def paged_attn_decode_noalloc(pool: Pool, q, block_table, seq_lens, max_seq_len,
     return out, lse
 
 
+def prefill_plan():
+    """(persistent CTAs, workspace bytes, leading bytes that must start zero)
+    of a prefill call on the current device."""
+    n, w, z = _I(), _SZ(), _SZ()
+    _check(_lib.pkv_prefill_plan(ctypes.byref(n), ctypes.byref(w), ctypes.byref(z)),
+           "pkv_prefill_plan")
+    return n.value, w.value, z.value
+
+
+def prefill_workspace(device="cuda"):
+    """A prefill workspace ready for its first call (counters zeroed).  Calls
+    leave it ready again, so it is meant to be kept and reused."""
+    _, nbytes, zbytes = prefill_plan()
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    ws[:zbytes].zero_()
+    return ws
+
+
 def paged_attn_prefill(pool: Pool, q, cu_q, block_table, seq_lens, max_q_len, softmax_scale,
-                       out=None, lse=None, want_lse=True, stream=None):
-    """Causal chunk attention: q [total_q][Hq][128] bf16 -> (out bf16, lse fp32)."""
+                       workspace=None, out=None, lse=None, want_lse=True, stream=None):
+    """Causal chunk attention: q [total_q][Hq][128] bf16 -> (out bf16, lse fp32).
+    `workspace` (from prefill_workspace()) is allocated when not given."""
     _need(q, torch.bfloat16, "q")
     for t, n in ((cu_q, "cu_q"), (block_table, "block_table"), (seq_lens, "seq_lens")):
         _need(t, torch.int32, n)
     T, Hq, _ = q.shape
+    if workspace is None:
+        workspace = prefill_workspace(q.device)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
     pc = pool.c()
     st = _lib.pkv_paged_attn_prefill(
-        ctypes.byref(pc), _ptr(q), _ptr(cu_q), seq_lens.shape[0], Hq, _ptr(block_table),
-        block_table.shape[1], _ptr(seq_lens), int(max_q_len), float(softmax_scale), _ptr(out),
-        _ptr(lse), _stream(stream))
+        ctypes.byref(pc), _ptr(q), T, _ptr(cu_q), seq_lens.shape[0], Hq, _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), int(max_q_len), float(softmax_scale),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+        _stream(stream))
     _check(st, "pkv_paged_attn_prefill")
     return out, lse
 

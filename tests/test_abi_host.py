@@ -142,13 +142,37 @@ def test_prefill_rejects_int8_pool_and_bad_arguments(lib):
     f.restype = ctypes.c_int32
     i8 = good_pool(dtype=1, k_scale=FAKE, v_scale=FAKE)
     V = ctypes.c_void_p
-    args = [V(FAKE), V(FAKE), 1, 4, V(FAKE), 4, V(FAKE), 16, ctypes.c_float(0.1), V(FAKE),
-            None, None]
+    plan = lib.pkv_prefill_plan
+    plan.restype = ctypes.c_int32
+    ctas, ws, zb = ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
+    assert plan(ctypes.byref(ctas), ctypes.byref(ws), ctypes.byref(zb)) == 0
+    assert ctas.value > 0
+    # counters (4 per CTA, whole 256-byte lines), then two slots per CTA of
+    # 256 rows x (128 + 1) fp32
+    assert zb.value == (16 * ctas.value + 255) // 256 * 256
+    assert ws.value == zb.value + 2 * ctas.value * 256 * 129 * 4
+    args = [V(FAKE), 16, V(FAKE), 1, 4, V(FAKE), 4, V(FAKE), 16, ctypes.c_float(0.1), V(FAKE),
+            ctypes.c_size_t(ws.value), V(FAKE), None, None]
     assert f(ctypes.byref(i8), *args) == UNSUPPORTED
     bf = good_pool()
     bad = list(args)
-    bad[3] = 3                                                  # Hq not a multiple of Hkv
+    bad[4] = 3                                                  # Hq not a multiple of Hkv
     assert f(ctypes.byref(bf), *bad) == INVALID
+    small = list(args)
+    small[11] = ctypes.c_size_t(ws.value - 16)                  # workspace too small
+    assert f(ctypes.byref(bf), *small) == INVALID
+    nows = list(args)
+    nows[10] = None                                             # no workspace
+    assert f(ctypes.byref(bf), *nows) == INVALID
+    odd = list(args)
+    odd[10] = V(FAKE + 8)                                       # workspace not 16-byte aligned
+    assert f(ctypes.byref(bf), *odd) == INVALID
+    neg = list(args)
+    neg[1] = -1                                                 # negative total_q
+    assert f(ctypes.byref(bf), *neg) == INVALID
+    none = list(args)
+    none[1] = 0                                                 # no query rows: nothing to do
+    assert f(ctypes.byref(bf), *none) == 0
 
 
 def test_status_strings(lib):

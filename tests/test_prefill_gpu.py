@@ -143,3 +143,51 @@ def test_empty_chunk_is_a_no_op(pk):
     ro, rl = ref(case, q, cu)
     check_out(out, ro, "empty chunk")
     check_lse(lse, rl, "empty chunk")
+
+
+def test_one_unit_split_over_many_ctas(pk):
+    """A single (sequence, tile pair, head) unit long enough to be cut over
+    about thirty CTAs: every part is merged by the log-sum-exp rule."""
+    rng = np.random.default_rng(65)
+    case, q, cu, mq = chunk_case(rng, [(256, 8192)], Hq=1, Hkv=1)
+    out, lse = run(pk, case, q, cu, mq)
+    ro, rl = ref(case, q, cu)
+    check_out(out, ro, "one unit, many parts")
+    check_lse(lse, rl, "one unit, many parts")
+
+
+def test_many_short_sequences(pk):
+    """Forty sequences of 1-300 rows: many segments per CTA, pairs whose
+    second tile is past the chunk, units cut anywhere."""
+    rng = np.random.default_rng(66)
+    qlens = rng.integers(1, 301, size=40)
+    shapes = [(int(n), int(n + rng.integers(0, 700))) for n in qlens]
+    case, q, cu, mq = chunk_case(rng, shapes, Hq=8, Hkv=2)
+    out, lse = run(pk, case, q, cu, mq)
+    ro, rl = ref(case, q, cu)
+    check_out(out, ro, "many short")
+    check_lse(lse, rl, "many short")
+
+
+def test_workspace_reuse_is_exact(pk):
+    """One workspace over a series of different calls gives the same bits as
+    a fresh workspace per call (the part counters return to zero), and the
+    same call twice gives the same bits (the merge order is fixed, whichever
+    CTA finishes last)."""
+    rng = np.random.default_rng(67)
+    calls = []
+    for shapes in ([(700, 3000)], [(256, 4096), (33, 90)], [(1000, 1000)]):
+        case, q, cu, mq = chunk_case(rng, shapes, Hq=8, Hkv=2)
+        pool = pk.Pool(dev_bf16(case.k_pool), dev_bf16(case.v_pool))
+        args = (pool, dev_bf16(q), dev(cu), dev(case.layout.block_table), dev(case.seq_lens),
+                mq, case.scale)
+        fresh = pk.paged_attn_prefill(*args)
+        calls.append((args, fresh))
+    ws = pk.prefill_workspace()
+    zero_bytes = pk.prefill_plan()[2]
+    for _ in range(2):
+        for args, (o0, l0) in calls:
+            o, l = pk.paged_attn_prefill(*args, workspace=ws)
+            assert torch.equal(o, o0) and torch.equal(l, l0)
+    assert pk.poll_device_error() == pk.OK
+    assert int(ws[:zero_bytes].count_nonzero()) == 0
