@@ -62,6 +62,9 @@ constexpr int NUM_THREADS = 320;              // softmax A: warps 0-3, B: 4-7, T
 // pipeline fill and drain, epilogue), and each CTA gets at least kMinCost.
 constexpr int kUnitCost0 = 4;
 constexpr int kMinCost = 2 * kUnitCost0;
+// Below this much work per CTA, cutting units costs more (storing and
+// merging parts) than it saves, and CTAs take whole units instead.
+constexpr int kSplitMinPerCta = 96;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S_A 0..127, S_B 128..255, O_A 256..383, O_B 384..511.  P of a
@@ -77,13 +80,11 @@ constexpr int OFF_V = OFF_K + NSTAGE * TILE;
 constexpr int OFF_BAR = OFF_V + NSTAGE * TILE;
 // barriers (pairs are per tile or per ring stage): q_full, q_empty, k_full,
 // k_empty, v_full, v_empty, s_full, p_full, o_done, drain, seg_full,
-// seg_empty, and per tile for a cut unit: epi (the tile's 4 warps are done
-// with the part), mrg (the tile's leader has counted it), st (the part is
-// stored), go (every other part is stored: merge)
+// seg_empty, and per tile for a cut unit: st (the tile's 4 warps have
+// stored their part), go (every other part is counted: merge)
 constexpr int BAR_QF = 0, BAR_QE = 2, BAR_KF = 4, BAR_KE = 6, BAR_VF = 8, BAR_VE = 10,
               BAR_SF = 12, BAR_PF = 14, BAR_OD = 16, BAR_DR = 18, BAR_SEGF = 19,
-              BAR_SEGE = 21, BAR_EPI = 23, BAR_MRG = 25, BAR_ST = 27, BAR_GO = 29,
-              NUM_BARS = 31;
+              BAR_SEGE = 21, BAR_ST = 23, BAR_GO = 25, NUM_BARS = 27;
 constexpr int NSEG = 2;                       // segment descriptor ring depth
 constexpr int OFF_SEG = OFF_BAR + 256;        // after the barriers (27 x 8 bytes)
 constexpr int OFF_MISC = OFF_SEG + NSEG * 64;
@@ -273,6 +274,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return __all_sync(0xffffffffu, ok);
 }
 
+// Adds to a counter in global memory after every write this thread has seen
+// (including other threads' writes ordered before it by a CTA barrier).
+__device__ __forceinline__ void red_release_add(uint32_t* ctr, uint32_t v) {
+  asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(ctr), "r"(v)
+               : "memory");
+}
+
 // Bounded wait (one thread) until a counter in global memory reaches target;
 // gpu-scope acquire, so what was written before the count is visible after.
 __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target,
@@ -298,19 +306,28 @@ __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target,
 // A unit is (sequence b, pair p of 128-row query tiles, query head hq); its
 // key blocks j = 0 .. nblk-1 cost one tile-block per tile that needs the
 // block (tile A needs blocks 0 .. nblk_a-1, tile B 0 .. nblk_b-1; nblk_b is
-// nblk_a or nblk_a + 1, or 0 when the pair's second tile is past the chunk).
+// nblk_a or nblk_a + 1, or 0 when the pair's second tile is past the chunk),
+// plus kUnitCost0 in front of block 0 for starting and finishing the unit.
 // Units are ordered by sequence, pairs from the last (heaviest) down, heads
 // innermost (the query heads of a KV head are neighbours, so they share K/V
 // through L2).  The total cost W is cut into Pe equal ranges, one per active
 // CTA (Pe = the grid, or fewer so that each range holds at least kMinCost);
 // a block belongs to the CTA whose range holds the block's starting cost
-// position.  A CTA therefore runs a sequence of segments (unit, blocks j0 ..
-// j1-1).  A range is at least 2 long and the block starts of a unit are at
-// most 2 apart, so the CTAs holding parts of one unit are consecutive: cf ..
-// cf + nown - 1; and since kMinCost exceeds the largest gap between block
-// starts (kUnitCost0 + 2), every active CTA has work.  The first part sits at
-// the end of CTA cf's range and goes to its tail slot 2 cf + 1; every other
-// part opens its CTA k's range and goes to its head slot 2 k.
+// position.  A range is at least 2 long and the block starts of a unit are
+// at most 2 apart, so the CTAs holding parts of one unit are consecutive,
+// cf .. cl; and since kMinCost exceeds the largest gap between block starts
+// (kUnitCost0 + 2), every active CTA has work.
+//
+// Each CTA walks its range backwards (units from its last position down),
+// so that for a unit cut between CTAs the part in CTA cl (the unit's last
+// blocks) is the last segment cl runs, while the part in any lower CTA k is
+// the first segment k runs.  CTA k < cl stores its part (normalised O and
+// log2-domain lse) in its workspace slot k and counts it; CTA cl, at the end
+// of its walk, waits until the cl - cf other parts are counted (they were
+// finished long before, by CTAs that started no later than it), then merges
+// them with its own part straight from TMEM and resets the count.  Waiting
+// only on lower CTAs, which the hardware starts first, keeps the wait safe
+// even if the grid were not resident all at once (it is: one CTA per SM).
 
 struct PairGeom {
   int q0, q_len, L, row0, rows_a, rows_b, pmin_a, nblk_a, nblk_b, nblk;
@@ -356,6 +373,14 @@ __device__ __forceinline__ int first_block_at(const PairGeom& g, long long off) 
   return j < g.nblk ? (int)j : g.nblk;
 }
 
+// a * b / c for non-negative a * b < 2^63, in 32-bit arithmetic when it fits
+__device__ __forceinline__ long long muldiv(long long a, long long b, long long c) {
+  const unsigned long long p = (unsigned long long)a * (unsigned long long)b;
+  if (p < (1ull << 32) && (unsigned long long)c < (1ull << 32))
+    return (long long)((uint32_t)p / (uint32_t)c);
+  return (long long)(p / (unsigned long long)c);
+}
+
 __device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, int b) {
   const int q0 = a.cu_q[b];
   const int q_len = a.cu_q[b + 1] - q0;
@@ -369,9 +394,9 @@ __device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, 
   return c * a.num_q_heads;
 }
 
-// Position of the work walk: unit (b, pair index pi, head hq) and block j.
+// Position of the work walk: unit (b, pair index pi, head hq).
 struct Cursor {
-  int b, pi, hq, j;
+  int b, pi, hq;
   long long ustart;             // cost position of the unit's first block
   PairGeom g;
   bool end;
@@ -388,37 +413,69 @@ __device__ __forceinline__ long long total_cost(const pkv_host::PrefillLaunch& a
   return t;
 }
 
-// The next unit (block 0) after the cursor's unit.
-__device__ __forceinline__ void next_unit(const pkv_host::PrefillLaunch& a, Cursor& c) {
-  c.ustart += unit_cost(c.g);
-  c.j = 0;
-  if (c.hq + 1 < a.num_q_heads) {
-    ++c.hq;
+// The unit before the cursor's unit (end if none).
+__device__ __forceinline__ void prev_unit(const pkv_host::PrefillLaunch& a, Cursor& c) {
+  if (c.hq > 0) {
+    --c.hq;
+    c.ustart -= unit_cost(c.g);
     return;
   }
-  c.hq = 0;
-  if (c.pi + 1 < n_pairs_of(c.g.q_len)) {
-    ++c.pi;
+  c.hq = a.num_q_heads - 1;
+  if (c.pi > 0) {
+    --c.pi;
     c.g = pair_geom(c.g.q0, c.g.q_len, c.g.L, pair_of(c));
+    c.ustart -= unit_cost(c.g);
     return;
   }
-  for (int b = c.b + 1; b < a.batch; ++b) {
+  for (int b = c.b - 1; b >= 0; --b) {
     const int q0 = a.cu_q[b], q_len = a.cu_q[b + 1] - q0, L = a.seq_lens[b];
     if (!seq_valid(a, q0, q_len, L) || q_len == 0) continue;
     c.b = b;
-    c.pi = 0;
-    c.g = pair_geom(q0, q_len, L, n_pairs_of(q_len) - 1);
+    c.pi = n_pairs_of(q_len) - 1;
+    c.g = pair_geom(q0, q_len, L, 0);
+    c.ustart -= unit_cost(c.g);
     return;
   }
   c.end = true;
 }
 
-// Cursor at the first block that starts at or after pos (0 <= pos < W), by
-// one warp (every lane gets the same cursor).
-__device__ __forceinline__ Cursor locate(const pkv_host::PrefillLaunch& a, long long pos, int lane) {
+// Moves the cursor n units forward (end if there are fewer).
+__device__ __forceinline__ void skip_units(const pkv_host::PrefillLaunch& a, Cursor& c, int n) {
+  while (n > 0 && !c.end) {
+    const int left = a.num_q_heads - c.hq;        // units left in this pair, this one included
+    if (n < left) {
+      c.hq += n;
+      c.ustart += (long long)n * unit_cost(c.g);
+      return;
+    }
+    n -= left;
+    c.ustart += (long long)left * unit_cost(c.g);
+    c.hq = 0;
+    if (c.pi + 1 < n_pairs_of(c.g.q_len)) {
+      ++c.pi;
+      c.g = pair_geom(c.g.q0, c.g.q_len, c.g.L, pair_of(c));
+      continue;
+    }
+    int b = c.b + 1;
+    for (; b < a.batch; ++b) {
+      const int q0 = a.cu_q[b], q_len = a.cu_q[b + 1] - q0, L = a.seq_lens[b];
+      if (!seq_valid(a, q0, q_len, L) || q_len == 0) continue;
+      c.b = b;
+      c.pi = 0;
+      c.g = pair_geom(q0, q_len, L, n_pairs_of(q_len) - 1);
+      break;
+    }
+    if (b >= a.batch) c.end = true;
+  }
+}
+
+// Cursor at the unit whose cost range holds pos (0 <= pos < W), by one warp
+// (every lane gets the same cursor).
+__device__ __forceinline__ Cursor locate_unit(const pkv_host::PrefillLaunch& a, long long pos,
+                                              int lane) {
   Cursor c;
   c.end = true;
-  c.b = c.pi = c.hq = c.j = 0;
+  c.b = c.pi = c.hq = 0;
   c.ustart = 0;
   long long base = 0;
   int bf = -1;
@@ -450,32 +507,23 @@ __device__ __forceinline__ Cursor locate(const pkv_host::PrefillLaunch& a, long 
     const PairGeom g = pair_geom(q0, q_len, L, np - 1 - pi);
     const long long cbp = (long long)unit_cost(g) * a.num_q_heads;
     if (pos < p0 + cbp) {
-      const long long rel = pos < p0 ? 0 : pos - p0;
       c.b = bf;
       c.pi = pi;
-      c.hq = (int)(rel / unit_cost(g));
+      c.hq = (int)muldiv(pos - p0, 1, unit_cost(g));
       c.ustart = p0 + (long long)c.hq * unit_cost(g);
       c.g = g;
-      c.j = first_block_at(g, pos - c.ustart);
       c.end = false;
       break;
     }
     p0 += cbp;
   }
-  if (!c.end && c.j >= c.g.nblk) next_unit(a, c);
   return c;
 }
 
-// Segment of the cursor's unit inside the cost range ending at hi: blocks
-// [c.j, returned j1).
-__device__ __forceinline__ int segment_end(const Cursor& c, long long hi) {
-  return first_block_at(c.g, hi - c.ustart);
-}
-
-__device__ __forceinline__ long long range_lo(long long W, int Pe, int k) { return W * k / Pe; }
+__device__ __forceinline__ long long range_lo(long long W, int Pe, int k) { return muldiv(W, k, Pe); }
 // the CTA whose range holds cost position pos
 __device__ __forceinline__ int owner_of(long long W, int Pe, long long pos) {
-  int k = (int)(pos * Pe / W);
+  int k = (int)muldiv(pos, Pe, W);
   while (k + 1 < Pe && range_lo(W, Pe, k + 1) <= pos) ++k;
   return k;
 }
@@ -497,9 +545,9 @@ static_assert(sizeof(SegDesc) == 64, "descriptor slot size");
 
 struct PrefillParams {
   pkv_host::PrefillLaunch a;
-  uint32_t* counters;           // [2][P][2] parts done, then parts stored, per (first CTA, tile)
-  float* ws_lse;                // [2P slots][2 tiles][128] log2-domain lse of a part
-  float4* ws_o;                 // [2P slots][2 tiles][32 channel quads][128 rows] normalised O
+  uint32_t* counters;           // [P][2] parts stored, per (first CTA of the unit, tile)
+  float* ws_lse;                // [P slots][2 tiles][128] log2-domain lse of a stored part
+  float4* ws_o;                 // [P slots][2 tiles][32 channel quads][128 rows] normalised O
 };
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -519,7 +567,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   SegDesc* seg_ring = reinterpret_cast<SegDesc*>(base + OFF_SEG);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_MISC);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(base + OFF_MISC + 4);
-  volatile uint32_t* merge_flag = reinterpret_cast<volatile uint32_t*>(base + OFF_MISC + 8);  // [2]
+
+  // The producer warp plans this CTA's walk while the barriers and TMEM are
+  // set up.  Split mode: the range is walked backwards, from the unit holding
+  // its last position down to the unit holding lo; within a unit, blocks j0
+  // .. j1-1 run in order.  Whole-unit mode: CTA c takes units c, 2P-1-c,
+  // 2P+c, ... (heaviest first, snaking so that the CTAs that took the
+  // heaviest units of one round take the lightest of the next).
+  long long W = 0, lo = 0, hi = 0;
+  bool split = false;
+  int Pe = P;
+  Cursor c;
+  c.end = true;
+  if (warp == WARP_TMA) {
+    // the first block's page ids of the first sequence: usually needed first
+    if (lane < BN / kPageSize && lane < a.max_pages)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + lane));
+    W = total_cost(a, lane);
+    split = W >= (long long)kSplitMinPerCta * P;
+    Pe = split ? active_ctas(W, P) : P;
+    if (split && cta < Pe) {
+      lo = range_lo(W, Pe, cta);
+      hi = range_lo(W, Pe, cta + 1);
+    }
+    if (split) {
+      if (lo < hi) c = locate_unit(a, hi - 1, lane);
+    } else if (W > 0) {
+      c = locate_unit(a, 0, lane);
+      skip_units(a, c, cta);
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
@@ -534,9 +611,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar(BAR_OD + x), 1);
       mbar_init(bar(BAR_SEGF + x), 1);
       mbar_init(bar(BAR_SEGE + x), 9);            // 8 softmax warps + the MMA warp
-      mbar_init(bar(BAR_EPI + x), 4);             // the tile's 4 softmax warps
-      mbar_init(bar(BAR_MRG + x), 1);
-      mbar_init(bar(BAR_ST + x), 4);
+      mbar_init(bar(BAR_ST + x), 4);              // the tile's 4 softmax warps
       mbar_init(bar(BAR_GO + x), 1);
     }
     mbar_init(bar(BAR_DR), 1);
@@ -559,24 +634,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1, nq_a = 0, nq_b = 0;
   if (warp == WARP_TMA) {
     // ------------------------------------------------ scheduler + producer
-    const long long W = total_cost(a, lane);
-    const int Pe = active_ctas(W, P);
-    long long lo = 0, hi = 0;
-    if (cta < Pe) {
-      lo = range_lo(W, Pe, cta);
-      hi = range_lo(W, Pe, cta + 1);
-    }
-    Cursor c;
-    c.end = true;
-    if (lo < hi) c = locate(a, lo, lane);
     bool ok = true;
     int t = 0;                                    // K/V blocks issued so far
     for (int sg = 0;; ++sg) {
-      const bool has = !c.end && c.ustart + block_off(c.g, c.j) < hi;
+      int j0 = 0, j1 = 0, cf = cta, nown = 1;
+      if (split) {
+        // the next unit (going down) with a block start in [lo, hi)
+        while (!c.end) {
+          j0 = first_block_at(c.g, lo - c.ustart);
+          j1 = first_block_at(c.g, hi - c.ustart);
+          if (j0 < j1) break;
+          if (c.ustart <= lo) c.end = true;
+          else prev_unit(a, c);
+        }
+        if (!c.end) {
+          cf = owner_of(W, Pe, c.ustart + block_off(c.g, 0));
+          nown = owner_of(W, Pe, c.ustart + block_off(c.g, c.g.nblk - 1)) - cf + 1;
+        }
+      } else if (!c.end) {
+        j1 = c.g.nblk;
+      }
+      const bool has = !c.end;
       const int ri = sg % NSEG;
       if (sg >= NSEG && !(ok = wait_bar(bar(BAR_SEGE + ri), ((sg / NSEG) - 1) & 1, abort_flag)))
         break;
-      const int j0 = c.j, j1 = has ? segment_end(c, hi) : 0;
       if (lane == 0) {
         SegDesc& d = seg_ring[ri];
         d.end = has ? 0 : 1;
@@ -591,9 +672,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           d.nblk_b = c.g.nblk_b;
           d.j0 = j0;
           d.j1 = j1;
-          const int cf = owner_of(W, Pe, c.ustart + block_off(c.g, 0));
           d.cf = cf;
-          d.nown = owner_of(W, Pe, c.ustart + block_off(c.g, c.g.nblk - 1)) - cf + 1;
+          d.nown = nown;
         }
         mbar_arrive(bar(BAR_SEGF + ri));          // release: the fields above are visible
       }
@@ -681,7 +761,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = j0 + 1; j < j1; ++j)
         if (!(ok = issue_kv(j, nothing))) break;
       if (!ok) break;
-      next_unit(a, c);
+      if (split) {
+        if (c.ustart <= lo) c.end = true;         // this unit opens the range: done
+        else prev_unit(a, c);
+      } else {
+        skip_units(a, c, (sg & 1) ? 2 * cta + 1 : 2 * P - 1 - 2 * cta);
+      }
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------- MMA issuer
@@ -785,8 +870,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float sl2 = a.softmax_scale * kLog2e;
     const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
-    // phase parities: s_full, o_done, epi/mrg, st, go
-    constexpr uint32_t PAR_S = 1, PAR_O = 2, PAR_C = 4, PAR_ST = 8, PAR_GO = 16;
+    // phase parities: s_full, o_done, st, go
+    constexpr uint32_t PAR_S = 1, PAR_O = 2, PAR_ST = 4, PAR_GO = 8;
     uint32_t par = 0;
     for (int sg = 0;; ++sg) {
       const int ri = sg % NSEG;
@@ -893,21 +978,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---- the whole unit ran here: normalise and store
         const size_t orow = ((size_t)(qrow0 + r) * Hq + hq) * kHeadDim;
         uint4* og = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
-#pragma unroll 1
-        for (int h = 0; h < 4; ++h) {
-          uint32_t o[32];
-          tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
-          tmem_wait_ld();
-          if (row_valid) {
+        uint32_t o[128];                          // the whole O row in one round trip
+        tmem_ld64(t_lane + tm_o(x), *reinterpret_cast<uint32_t(*)[64]>(&o[0]));
+        tmem_ld64(t_lane + tm_o(x) + 64, *reinterpret_cast<uint32_t(*)[64]>(&o[64]));
+        tmem_wait_ld();
+        if (row_valid) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
-              og[4 * h + k] = v;
-            }
+          for (int k = 0; k < 16; ++k) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * k + 0]) * inv, __uint_as_float(o[8 * k + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * k + 2]) * inv, __uint_as_float(o[8 * k + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * k + 4]) * inv, __uint_as_float(o[8 * k + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * k + 6]) * inv, __uint_as_float(o[8 * k + 7]) * inv);
+            og[k] = v;
           }
         }
         if (row_valid && a.lse)
@@ -916,128 +999,111 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
 
-      // ---- one part of a unit cut between CTAs.  The part is counted first;
-      // the last part to be counted merges all of them (its own straight from
-      // TMEM), every other part is stored to the workspace and then counted
-      // as stored, which the merging CTA waits for (those CTAs are running:
-      // they have counted their part, and storing it needs nothing else).
+      // ---- one part of a unit cut between CTAs cf .. cl.  A CTA below cl
+      // stores its part in its slot and counts it; CTA cl (this is its last
+      // segment) waits for the count, then merges.
       const int cf = d->cf;
-      uint32_t* ctr_done = prm.counters + 2 * cf + x;
-      uint32_t* ctr_stored = prm.counters + 2 * P + 2 * cf + x;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_EPI + x));
-      if (quarter == 0) {
-        if (!(ok = wait_bar(bar(BAR_EPI + x), (par & PAR_C) ? 1u : 0u, abort_flag))) break;
-        if (lane == 0) {
-          merge_flag[x] = atomicAdd(ctr_done, 1u) == (uint32_t)(nown - 1) ? 1u : 0u;
-          mbar_arrive(bar(BAR_MRG + x));
-        }
-      }
-      if (!(ok = wait_bar(bar(BAR_MRG + x), (par & PAR_C) ? 1u : 0u, abort_flag))) break;
-      par ^= PAR_C;
-      if (!merge_flag[x]) {
-        const size_t prow = (size_t)((2 * cta + (cta == cf ? 1 : 0)) * 2 + x);
+      const int cl = cf + nown - 1;
+      uint32_t* ctr = prm.counters + 2 * cf + x;
+      if (cta != cl) {
+        const size_t prow = (size_t)(cta * 2 + x);
         if (own) {
           float4* wo = prm.ws_o + prow * 32 * BM + r;
-#pragma unroll 1
-          for (int h = 0; h < 4; ++h) {
-            uint32_t o[32];
-            tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
-            tmem_wait_ld();
+          uint32_t o[128];                        // the whole O row in one round trip
+          tmem_ld64(t_lane + tm_o(x), *reinterpret_cast<uint32_t(*)[64]>(&o[0]));
+          tmem_ld64(t_lane + tm_o(x) + 64, *reinterpret_cast<uint32_t(*)[64]>(&o[64]));
+          tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              wo[(8 * h + k) * BM] =
-                  make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                              __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
-          }
+          for (int k = 0; k < 32; ++k)
+            wo[k * BM] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                                     __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
           prm.ws_lse[prow * BM + r] = m_run + fast_log2(l_run);
         } else {
           prm.ws_lse[prow * BM + r] = -INFINITY;  // no key of this tile in this part
         }
-        __threadfence();
+        // the tile's 4 warps have stored: one thread releases the count
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(BAR_ST + x));
         if (quarter == 0) {
           if (!(ok = wait_bar(bar(BAR_ST + x), (par & PAR_ST) ? 1u : 0u, abort_flag))) break;
-          if (lane == 0) {
-            __threadfence();
-            atomicAdd(ctr_stored, 1u);
-          }
+          if (lane == 0) red_release_add(ctr, 1u);
         }
         par ^= PAR_ST;
         release();
         continue;
       }
-      // the last part: wait until every other part is stored, then merge
+      // the merging CTA: wait until the cl - cf other parts are counted
       if (quarter == 0 && lane == 0) {
-        if (wait_count(ctr_stored, (uint32_t)(nown - 1), abort_flag)) {
-          *ctr_done = 0u;                         // ready for the next call
-          *ctr_stored = 0u;
+        if (wait_count(ctr, (uint32_t)(nown - 1), abort_flag)) {
+          *ctr = 0u;                              // ready for the next call
           mbar_arrive(bar(BAR_GO + x));
         }
       }
       __syncwarp();
       if (!(ok = wait_bar(bar(BAR_GO + x), (par & PAR_GO) ? 1u : 0u, abort_flag))) break;
       par ^= PAR_GO;
-      __threadfence();
-      // Parts of CTAs cf .. cf + nown - 1: cf's tail slot, the head slot of
-      // every later CTA, this CTA's own part from TMEM.  Every part enters as
-      // the stored parts do (O / l rounded to fp32, lse = m + log2 l), in CTA
-      // order, so the result does not depend on which CTA merges.
+      // Parts of CTAs cf .. cl: slot k for k < cl, this CTA's own part from
+      // TMEM.  Every part enters as the stored parts do (O / l rounded to
+      // fp32, lse = m + log2 l), in CTA order.
       const float lse_own = own ? m_run + fast_log2(l_run) : -INFINITY;
       auto part_lse = [&](int k) -> float {
         if (k == cta) return lse_own;
-        const int sk = k == cf ? 2 * cf + 1 : 2 * k;
-        return __ldcg(prm.ws_lse + (size_t)(sk * 2 + x) * BM + r);
+        return __ldcg(prm.ws_lse + (size_t)(k * 2 + x) * BM + r);
       };
       float M = -INFINITY;
+#pragma unroll 4
       for (int k = cf; k < cf + nown; ++k) M = fmaxf(M, part_lse(k));
+      // a part without keys of this row has lse -inf (weight 0) and no O
+      auto weight = [&](float ls) { return ls == -INFINITY ? 0.f : fast_exp2(ls - M); };
       float sum = 0.f;
+#pragma unroll 4
+      for (int k = cf; k < cf + nown; ++k) sum += weight(part_lse(k));
       const size_t orow = ((size_t)(qrow0 + r) * Hq + hq) * kHeadDim;
       uint4* og = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow);
 #pragma unroll 1
-      for (int h = 0; h < 4; ++h) {             // 32 channels at a time
-        float acc[32];
+      for (int h = 0; h < 2; ++h) {             // 64 channels at a time
+        float acc[64];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+        for (int i = 0; i < 64; ++i) acc[i] = 0.f;
         for (int k = cf; k < cf + nown; ++k) {
-          const float ls = part_lse(k);
-          const float f = ls == -INFINITY ? 0.f : fast_exp2(ls - M);   // 0: no keys, no O
-          if (h == 0) sum += f;
+          const float f = weight(part_lse(k));
           if (k == cta) {
             if (own) {                            // warp-uniform
-              uint32_t o[32];
-              tmem_ld32(t_lane + tm_o(x) + 32 * h, o);
+              uint32_t o[64];
+              tmem_ld64(t_lane + tm_o(x) + 64 * h, o);
               tmem_wait_ld();
+              // f == 0: no key of this row in this part (l = 0, O / l = NaN)
               if (f != 0.f) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) acc[i] = fmaf(f, __uint_as_float(o[i]) * inv, acc[i]);
+                for (int i = 0; i < 64; ++i) acc[i] = fmaf(f, __uint_as_float(o[i]) * inv, acc[i]);
               }
             }
-          } else if (f != 0.f) {
-            const size_t pk = (size_t)((k == cf ? 2 * cf + 1 : 2 * k) * 2 + x);
-            float4 v[8];
+          } else {
+            const size_t pk = (size_t)(k * 2 + x);
+            float4 v[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __ldcg(prm.ws_o + (pk * 32 + 8 * h + i) * BM + r);
+            for (int i = 0; i < 16; ++i) v[i] = __ldcg(prm.ws_o + (pk * 32 + 16 * h + i) * BM + r);
+            if (f != 0.f) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              acc[4 * i + 0] = fmaf(f, v[i].x, acc[4 * i + 0]);
-              acc[4 * i + 1] = fmaf(f, v[i].y, acc[4 * i + 1]);
-              acc[4 * i + 2] = fmaf(f, v[i].z, acc[4 * i + 2]);
-              acc[4 * i + 3] = fmaf(f, v[i].w, acc[4 * i + 3]);
+              for (int i = 0; i < 16; ++i) {
+                acc[4 * i + 0] = fmaf(f, v[i].x, acc[4 * i + 0]);
+                acc[4 * i + 1] = fmaf(f, v[i].y, acc[4 * i + 1]);
+                acc[4 * i + 2] = fmaf(f, v[i].z, acc[4 * i + 2]);
+                acc[4 * i + 3] = fmaf(f, v[i].w, acc[4 * i + 3]);
+              }
             }
           }
         }
         const float is = sum > 0.f ? 1.0f / sum : 0.f;
         if (row_valid) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 8; ++i) {
             uint4 w;
             w.x = pack_bf16x2(acc[8 * i + 0] * is, acc[8 * i + 1] * is);
             w.y = pack_bf16x2(acc[8 * i + 2] * is, acc[8 * i + 3] * is);
             w.z = pack_bf16x2(acc[8 * i + 4] * is, acc[8 * i + 5] * is);
             w.w = pack_bf16x2(acc[8 * i + 6] * is, acc[8 * i + 7] * is);
-            og[4 * h + i] = w;
+            og[8 * h + i] = w;
           }
         }
       }
@@ -1116,8 +1182,8 @@ bool encode_q_map(CUtensorMap* m, const void* q, int total_q, int hq) {
 }
 
 // Workspace: per-(CTA, tile) part counters, then the parts' lse, then their O.
-size_t ws_counter_bytes(int ctas) { return ((size_t)4 * ctas * 4 + 255) / 256 * 256; }
-size_t ws_lse_bytes(int ctas) { return (size_t)2 * ctas * SLOT_ROWS * 4; }
+size_t ws_counter_bytes(int ctas) { return ((size_t)2 * ctas * 4 + 255) / 256 * 256; }
+size_t ws_lse_bytes(int ctas) { return (size_t)ctas * SLOT_ROWS * 4; }
 
 }  // namespace
 
@@ -1150,7 +1216,7 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
 int prefill_ctas(int sms) { return sms < kMaxPrefillCtas ? sms : kMaxPrefillCtas; }
 
 size_t prefill_workspace_bytes(int ctas) {
-  return ws_counter_bytes(ctas) + ws_lse_bytes(ctas) + (size_t)2 * ctas * SLOT_ROWS * kHeadDim * 4;
+  return ws_counter_bytes(ctas) + ws_lse_bytes(ctas) + (size_t)ctas * SLOT_ROWS * kHeadDim * 4;
 }
 
 size_t prefill_workspace_zero_bytes(int ctas) { return ws_counter_bytes(ctas); }

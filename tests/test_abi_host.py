@@ -147,10 +147,10 @@ def test_prefill_rejects_int8_pool_and_bad_arguments(lib):
     ctas, ws, zb = ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
     assert plan(ctypes.byref(ctas), ctypes.byref(ws), ctypes.byref(zb)) == 0
     assert ctas.value > 0
-    # counters (4 per CTA, whole 256-byte lines), then two slots per CTA of
+    # counters (2 per CTA, whole 256-byte lines), then one slot per CTA of
     # 256 rows x (128 + 1) fp32
-    assert zb.value == (16 * ctas.value + 255) // 256 * 256
-    assert ws.value == zb.value + 2 * ctas.value * 256 * 129 * 4
+    assert zb.value == (8 * ctas.value + 255) // 256 * 256
+    assert ws.value == zb.value + ctas.value * 256 * 129 * 4
     args = [V(FAKE), 16, V(FAKE), 1, 4, V(FAKE), 4, V(FAKE), 16, ctypes.c_float(0.1), V(FAKE),
             ctypes.c_size_t(ws.value), V(FAKE), None, None]
     assert f(ctypes.byref(i8), *args) == UNSUPPORTED

@@ -182,6 +182,10 @@ def test_workspace_reuse_is_exact(pk):
         args = (pool, dev_bf16(q), dev(cu), dev(case.layout.block_table), dev(case.seq_lens),
                 mq, case.scale)
         fresh = pk.paged_attn_prefill(*args)
+        assert pk.poll_device_error() == pk.OK
+        ro, rl = ref(case, q, cu)
+        check_out(fresh[0], ro, f"reuse {shapes}")
+        check_lse(fresh[1], rl, f"reuse {shapes}")
         calls.append((args, fresh))
     ws = pk.prefill_workspace()
     zero_bytes = pk.prefill_plan()[2]
