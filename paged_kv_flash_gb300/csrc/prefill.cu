@@ -692,7 +692,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // `between`) the V boxes.  Lane i < 8 loads page i of the block (both
       // 64-channel halves), so a block takes four TMA instructions, and the
       // next block's page ids are read while this block's waits run.
-      int pg_next = page_ids(j0);
+      auto nothing = []() { return true; };
+      int pg_next = 0;
       auto issue_kv = [&](int j, auto&& between) -> bool {
         const int st = t % NSTAGE;
         int pg = pg_next;
@@ -755,9 +756,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         return true;
       };
-      auto nothing = []() { return true; };
-
-      if (!(ok = issue_kv(j0, issue_q))) break;
+      // The first segment has nothing in flight: its Q goes out first, in
+      // parallel with the page-id read for its first block.
+      if (sg == 0 && !(ok = issue_q())) break;
+      pg_next = page_ids(j0);
+      auto later_q = [&]() { return sg == 0 || issue_q(); };
+      if (!(ok = issue_kv(j0, later_q))) break;
       for (int j = j0 + 1; j < j1; ++j)
         if (!(ok = issue_kv(j, nothing))) break;
       if (!ok) break;
