@@ -169,17 +169,17 @@ class Mixed:
                 q_chunk=to_dev_bf16(torch, s.q_chunk), q_dec=to_dev_bf16(torch, s.q_decode),
                 cu_q=to_dev(torch, W.cu_from_counts([s.chunk_len])),
                 lens_p=to_dev(torch, np.array([s.prefill_len], np.int32)),
-                lens_d=to_dev(torch, s.decode_lens), chunk_len=s.chunk_len,
+                lens_d=to_dev(torch, s.decode_lens), chunk_len=s.chunk_len, context=s.prefill_len,
                 max_dec=int(s.decode_lens.max()),
                 flops=prefill_flops(s.chunk_len, s.prefill_len, wl.Hq),
                 dbytes=decode_bytes(s.decode_lens, wl.Hkv),
                 host=s)
-            S, C, ws = pk.decode_plan(self.R, wl.Hq, wl.Hkv, st["max_dec"])
+            S, C, ws, _ = pk.decode_plan(self.R, wl.Hq, wl.Hkv, st["max_dec"])
             st["splits"] = S
             st["launches"] = 3 + (1 if S > 1 else 0)
             self.steps.append(st)
-        ws_max = max(pk.decode_plan(self.R, wl.Hq, wl.Hkv, s["max_dec"])[2] for s in self.steps)
-        self.ws = torch.empty(max(ws_max, 256), dtype=torch.uint8, device="cuda")
+        plans = [pk.decode_plan(self.R, wl.Hq, wl.Hkv, s["max_dec"]) for s in self.steps]
+        self.ws = pk.decode_workspace(max(p[2] for p in plans), max(p[3] for p in plans))
         self.ws_p = pk.prefill_workspace()
         T = max(s["chunk_len"] for s in self.steps)
         self.out_p = torch.empty((T, wl.Hq, D), dtype=torch.bfloat16, device="cuda")
@@ -239,20 +239,35 @@ def time_mixed(torch, pk, mixed, K, Wu, world, rank):
     app_ms = pre_ms = dec_ms = 0.0
     flops = dbytes = 0.0
     launches = 0
-    pre_launch_ms = []
+    # per chunk of the prompt (step i runs chunk i mod 14): summed times, count
+    per = [[0.0, 0.0, 0.0, 0] for _ in range(nsteps)]
     for i in range(K):
         e = evs[i]
-        st = mixed.steps[(Wu + i) % nsteps]
-        app_ms += e[0].elapsed_time(e[1])
-        p = e[1].elapsed_time(e[2])
+        c = (Wu + i) % nsteps
+        st = mixed.steps[c]
+        a, p, d = e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])
+        app_ms += a
         pre_ms += p
-        pre_launch_ms.append(p)
-        dec_ms += e[2].elapsed_time(e[3])
+        dec_ms += d
+        per[c][0] += a
+        per[c][1] += p
+        per[c][2] += d
+        per[c][3] += 1
         flops += st["flops"]
         dbytes += st["dbytes"]
         launches += st["launches"]
+    chunks = []
+    for c, (a, p, d, n) in enumerate(per):
+        if not n:
+            continue
+        st = mixed.steps[c]
+        chunks.append({"chunk": c, "rows": st["chunk_len"], "context": st["context"],
+                       "append_us": round(a * 1e3 / n, 2), "prefill_us": round(p * 1e3 / n, 2),
+                       "prefill_TFLOPs": round(st["flops"] / (p * 1e-3 / n) / 1e12, 1),
+                       "decode_us": round(d * 1e3 / n, 2),
+                       "decode_GBps": round(st["dbytes"] / (d * 1e-3 / n) / 1e9, 1)})
     return dict(total_ms=total_ms, app_ms=app_ms, pre_ms=pre_ms, dec_ms=dec_ms, flops=flops,
-                dbytes=dbytes, launches=launches, clocks=clk)
+                dbytes=dbytes, launches=launches, clocks=clk, chunks=chunks)
 
 
 def time_e2e(torch, pk, mixed, K):
@@ -344,23 +359,25 @@ def other_configs(torch, pk, hbm, bf16):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     res = {}
 
-    def decode_entry(name, case, pool, per_pos, smooth=None, graph=False):
+    def decode_entry(name, case, pool, per_pos, smooth=None, graph=False, fused=False):
         q = to_dev_bf16(torch, case.q)
         bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
         ms = int(case.seq_lens.max())
-        S, C, wsb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
-        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+        S, C, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
+        ws = pk.decode_workspace(wsb, zb)
         out = torch.empty_like(q)
         lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
         w = to_dev(torch, smooth) if smooth is not None else None
         fn = lambda: pk.paged_attn_decode(pool, q, bt, sl, ms, SCALE, k_smooth=w, workspace=ws,
-                                          out=out, lse=lse)
+                                          out=out, lse=lse, fused=fused)
         med, mn = time_events(torch, fn, flush=flush)
         byts = decode_bytes(case.seq_lens, case.Hkv, per_pos)
         r = {"us": round(med, 2), "us_min": round(mn, 2), "GBps": round(byts / med / 1e3, 1),
              "frac_of_8TBps": round(byts / med / 1e3 / NOMINAL_HBM_GBS, 4),
              "frac_of_measured": round(byts / med / 1e3 / hbm, 4), "bytes": int(byts),
              "splits": S, "cold_l2": True}
+        if fused:
+            r["note"] = "combine fused into the split kernel (pkv_paged_attn_decode_fused)"
         if graph:
             g = time_graph(torch, fn)
             r["graph_us_per_launch"] = round(g, 2)
@@ -369,13 +386,14 @@ def other_configs(torch, pk, hbm, bf16):
         assert pk.poll_device_error() == pk.OK
 
     c1 = W.decode_1k()
-    decode_entry("decode_1k_b1_gqa16x8", c1,
-                 pk.Pool(to_dev_bf16(torch, c1.k_pool), to_dev_bf16(torch, c1.v_pool)), 512,
-                 graph=True)
+    p1 = pk.Pool(to_dev_bf16(torch, c1.k_pool), to_dev_bf16(torch, c1.v_pool))
+    decode_entry("decode_1k_b1_gqa16x8", c1, p1, 512, graph=True)
+    decode_entry("decode_1k_b1_gqa16x8_fused", c1, p1, 512, graph=True, fused=True)
     c3 = W.batched_decode()
-    decode_entry("batched_decode_b64_gqa32x8", c3,
-                 pk.Pool(to_dev_bf16(torch, c3.k_pool), to_dev_bf16(torch, c3.v_pool)), 512)
-    del c3
+    p3 = pk.Pool(to_dev_bf16(torch, c3.k_pool), to_dev_bf16(torch, c3.v_pool))
+    decode_entry("batched_decode_b64_gqa32x8", c3, p3, 512)
+    decode_entry("batched_decode_b64_gqa32x8_fused", c3, p3, 512, fused=True)
+    del c3, p3
     for B in (1, 8):
         app, q = W.int8_long_decode(B=B)
         pool = pk.Pool.empty(app.layout.num_pages, app.Hkv, dtype=torch.int8)
@@ -525,8 +543,8 @@ def profile_case(torch, pk, name, reps=3):
         q = to_dev_bf16(torch, case.q)
         bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
         ms = int(case.seq_lens.max())
-        _, _, wsb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
-        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+        _, _, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
+        ws = pk.decode_workspace(wsb, zb)
         out = torch.empty_like(q)
         lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
         fn = lambda: pk.paged_attn_decode(pool, q, bt, sl, ms, SCALE, k_smooth=w, workspace=ws,
@@ -650,6 +668,13 @@ def main():
                     "frac_of_measured_burst": round(pre_tflops / bf16, 4),
                     "flops_per_step": round(r["flops"] / K)},
         "append": {"us_per_step": round(r["app_ms"] * 1e3 / K, 2)},
+        # the 14 steps of one pass over the prompt (each the mean over the
+        # timed steps that ran that chunk), and their sum
+        "steps": r["chunks"],
+        "prompt_pass": {"prefill_us": round(sum(c["prefill_us"] for c in r["chunks"]), 1),
+                        "decode_us": round(sum(c["decode_us"] for c in r["chunks"]), 1),
+                        "append_us": round(sum(c["append_us"] for c in r["chunks"]), 1),
+                        "chunks": len(r["chunks"])},
         "roofline": {"kernel": "prefill_kernel (tcgen05)", "bound": "tensor",
                      "achieved": round(pre_tflops, 1), "peak": bf16_sus, "unit": "TFLOP/s",
                      "frac": round(frac, 4), "traffic": PREFILL_TRAFFIC_BYTES,

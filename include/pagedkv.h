@@ -105,17 +105,23 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
  * num_splits 0 asks for the built-in heuristic (split count chosen from the
  * batch, the heads and the device's SM count), > 0 forces that many splits.
  * Outputs (host pointers, each may be NULL): the split count S, the pages per
- * split, and the workspace bytes the decode call needs (0 when S == 1).
+ * split, the workspace bytes the decode call needs (0 when S == 1), and how
+ * many leading bytes of that workspace must be zero before its first use
+ * (256 KiB of part counters when S > 1, else 0).  More than 65,536
+ * (sequence, KV head) pairs are never split by the heuristic, and a forced
+ * num_splits > 1 for them is PKV_ERR_INVALID.
  */
 pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                            int32_t max_seq_len, int32_t num_splits, int32_t* splits_out,
-                           int32_t* pages_per_split_out, size_t* workspace_bytes_out);
+                           int32_t* pages_per_split_out, size_t* workspace_bytes_out,
+                           size_t* zero_bytes_out);
 
 /*
  * paged_attn_decode -- one query token per sequence against its cached
  * positions 0 .. seq_lens[b]-1 (the token's own position included): split-KV
  * partials, then a log-sum-exp combine ("Fused kernels ...": online softmax
- * over the pages in place, split-KV for decode, separate combine kernel).
+ * over the pages in place, split-KV for decode, separate combine kernel).  A
+ * row whose keys fit one split is finished by that split.
  *
  *  q            bf16 [batch][num_q_heads][128].
  *  block_table  int32 [batch][max_pages]; seq_lens int32 [batch] (device);
@@ -123,9 +129,10 @@ pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_he
  *  k_smooth     INT8 pools: the same fp32 [128] weight given to kv_append,
  *               or NULL if the keys were not smoothed; NULL for bf16.
  *  num_splits   0 = heuristic, > 0 forces (see pkv_decode_plan).
- *  workspace    fp32 scratch of at least pkv_decode_plan's bytes (256-byte
+ *  workspace    scratch of at least pkv_decode_plan's bytes (256-byte
  *               aligned), may be NULL when that is 0.  Holds the split
- *               partials; its contents are dead after the call.
+ *               partials; its contents are dead after the call (its first
+ *               zero_bytes are not used by this call).
  *  out          bf16 [batch][num_q_heads][128]; lse fp32 [batch][num_q_heads]
  *               or NULL.
  */
@@ -135,6 +142,31 @@ pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t ba
                                  int32_t max_seq_len, float softmax_scale,
                                  const float* k_smooth, int32_t num_splits, void* workspace,
                                  size_t workspace_bytes, void* out, float* lse, void* stream);
+
+/*
+ * paged_attn_decode_fused -- the same decode with the combine fused into the
+ * split kernel ("Not kept: the attention combine fused into the split-KV
+ * kernel", re-measured on GB300; the separate combine above stays the
+ * default because it is faster there except on a single cold launch).  Each
+ * split stores its partial and counts it with an acquire-release atomic; the
+ * split that completes the count of a (sequence, KV head) merges the partials
+ * in split order (bit-identical to the separate combine) and resets the
+ * count.  No split waits on another.
+ *
+ * Arguments: as pkv_paged_attn_decode.  The workspace's first zero_bytes
+ * (pkv_decode_plan) hold the part counters: they must be zero before the
+ * first use; every call that completes leaves them zero again, so a
+ * workspace is zeroed once and reused by calls of any shape that fits it
+ * (zero it again after PKV_ERR_TIMEOUT).  Calls sharing a workspace must not
+ * overlap.
+ */
+pkv_status pkv_paged_attn_decode_fused(const pkv_pool* pool, const void* q, int32_t batch,
+                                       int32_t num_q_heads, const int32_t* block_table,
+                                       int32_t max_pages, const int32_t* seq_lens,
+                                       int32_t max_seq_len, float softmax_scale,
+                                       const float* k_smooth, int32_t num_splits,
+                                       void* workspace, size_t workspace_bytes, void* out,
+                                       float* lse, void* stream);
 
 /*
  * paged_attn_decode_noalloc -- the same decode as pkv_paged_attn_decode for
@@ -157,7 +189,8 @@ pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t ba
  * fit in 16 MiB the split count is lowered until they do (the result differs
  * from pkv_paged_attn_decode only by rounding).  A forced num_splits whose
  * partials need more than 16 MiB (batch * num_q_heads * num_splits * 516 bytes
- * plus alignment) is rejected with PKV_ERR_INVALID before any launch.
+ * plus alignment and 256 KiB the plan reserves) is rejected with
+ * PKV_ERR_INVALID before any launch.
  *
  * The first call on each device looks the array's device address up with
  * cudaGetSymbolAddress (once per device, with that device current); make

@@ -63,9 +63,16 @@ pkv_status check_pool(const pkv_pool* pool) {
 constexpr long long kPlanSlotsNum = 4, kPlanSlotsDen = 5;   // 0.8 CTAs per slot
 constexpr long long kPlanMinPages = 8, kPlanMaxPages = 128;
 
+// Workspace (splits > 1): part counters u32 [kDecodeCounters] indexed by
+// b * Hkv + h (a fixed region, so that a workspace reused by calls of any
+// shape never finds partials where counters go; zero between calls), then
+// normalised partial O fp32 [B][Hq][S][128], then log2 lse fp32 [B][Hq][S],
+// each 256-byte aligned.  With more than kDecodeCounters (sequence, KV head)
+// pairs the heuristic does not split (there is parallelism enough).
+constexpr long long kDecodeCounters = 65536;
 struct Plan {
   int splits, pages_per_split;
-  size_t ws_bytes, ws_lse_offset;
+  size_t ws_bytes, ws_zero_bytes, ws_o_offset, ws_lse_offset;
 };
 
 Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, int num_splits) {
@@ -83,22 +90,31 @@ Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, in
     C = (int)std::min<long long>(c, mp);
   }
   C = std::max(1, C);
+  if (num_splits == 0 && (long long)batch * num_kv_heads > kDecodeCounters) C = mp;
   Plan p;
   p.splits = (mp + C - 1) / C;
   p.pages_per_split = C;
   if (p.splits == 1) {
-    p.ws_bytes = 0;
-    p.ws_lse_offset = 0;
+    p.ws_bytes = p.ws_zero_bytes = p.ws_o_offset = p.ws_lse_offset = 0;
   } else {
     const size_t rows = (size_t)batch * num_q_heads * p.splits;
     const size_t o_bytes = rows * pkv::kHeadDim * sizeof(float);
-    p.ws_lse_offset = (o_bytes + 255) / 256 * 256;
+    p.ws_zero_bytes = (size_t)kDecodeCounters * sizeof(uint32_t);
+    p.ws_o_offset = p.ws_zero_bytes;
+    p.ws_lse_offset = p.ws_o_offset + (o_bytes + 255) / 256 * 256;
     p.ws_bytes = p.ws_lse_offset + (rows * sizeof(float) + 255) / 256 * 256;
   }
   return p;
 }
 
 pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+void set_workspace(pkv_host::DecodeLaunch& a, const Plan& p, void* ws, bool fused) {
+  char* base = static_cast<char*>(ws);
+  a.ws_ctr = p.ws_bytes && fused ? reinterpret_cast<uint32_t*>(base) : nullptr;
+  a.ws_o = p.ws_bytes ? reinterpret_cast<float*>(base + p.ws_o_offset) : nullptr;
+  a.ws_lse = p.ws_bytes ? reinterpret_cast<float*>(base + p.ws_lse_offset) : nullptr;
+}
 
 }  // namespace
 
@@ -126,23 +142,26 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
 
 pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                            int32_t max_seq_len, int32_t num_splits, int32_t* splits_out,
-                           int32_t* pages_per_split_out, size_t* workspace_bytes_out) {
+                           int32_t* pages_per_split_out, size_t* workspace_bytes_out,
+                           size_t* zero_bytes_out) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
       max_seq_len < 0 || num_splits < 0)
     return PKV_ERR_INVALID;
+  if (num_splits > 1 && (long long)batch * num_kv_heads > kDecodeCounters) return PKV_ERR_INVALID;
   const Plan p = make_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits);
   if (splits_out) *splits_out = p.splits;
   if (pages_per_split_out) *pages_per_split_out = p.pages_per_split;
   if (workspace_bytes_out) *workspace_bytes_out = p.ws_bytes;
+  if (zero_bytes_out) *zero_bytes_out = p.ws_zero_bytes;
   return PKV_OK;
 }
 
-pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t batch,
-                                 int32_t num_q_heads, const int32_t* block_table,
-                                 int32_t max_pages, const int32_t* seq_lens,
-                                 int32_t max_seq_len, float softmax_scale,
-                                 const float* k_smooth, int32_t num_splits, void* workspace,
-                                 size_t workspace_bytes, void* out, float* lse, void* stream) {
+static pkv_status decode_call(const pkv_pool* pool, const void* q, int32_t batch,
+                              int32_t num_q_heads, const int32_t* block_table, int32_t max_pages,
+                              const int32_t* seq_lens, int32_t max_seq_len, float softmax_scale,
+                              const float* k_smooth, int32_t num_splits, void* workspace,
+                              size_t workspace_bytes, void* out, float* lse, void* stream,
+                              bool fused) {
   pkv_status st = check_pool(pool);
   if (st != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads || max_pages <= 0 ||
@@ -154,6 +173,8 @@ pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t ba
   if (batch == 0) return PKV_OK;
   if (!q || !block_table || !seq_lens || !out) return PKV_ERR_INVALID;
   if (pool->dtype == PKV_BF16 && k_smooth) return PKV_ERR_INVALID;
+  if (num_splits > 1 && (long long)batch * pool->num_kv_heads > kDecodeCounters)
+    return PKV_ERR_INVALID;
   const Plan p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, num_splits);
   if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned(workspace, 256)))
     return PKV_ERR_INVALID;
@@ -175,14 +196,34 @@ pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t ba
   a.k_smooth = k_smooth;
   a.splits = p.splits;
   a.pages_per_split = p.pages_per_split;
-  a.ws_o = p.ws_bytes ? static_cast<float*>(workspace) : nullptr;
-  a.ws_lse = p.ws_bytes
-                 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + p.ws_lse_offset)
-                 : nullptr;
+  set_workspace(a, p, workspace, fused);
   a.out = out;
   a.lse = lse;
   return cuda_status(pkv_host::launch_decode(a, pool->dtype == PKV_INT8,
                                              static_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_attn_decode(const pkv_pool* pool, const void* q, int32_t batch,
+                                 int32_t num_q_heads, const int32_t* block_table,
+                                 int32_t max_pages, const int32_t* seq_lens,
+                                 int32_t max_seq_len, float softmax_scale,
+                                 const float* k_smooth, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, void* out, float* lse, void* stream) {
+  return decode_call(pool, q, batch, num_q_heads, block_table, max_pages, seq_lens, max_seq_len,
+                     softmax_scale, k_smooth, num_splits, workspace, workspace_bytes, out, lse,
+                     stream, false);
+}
+
+pkv_status pkv_paged_attn_decode_fused(const pkv_pool* pool, const void* q, int32_t batch,
+                                       int32_t num_q_heads, const int32_t* block_table,
+                                       int32_t max_pages, const int32_t* seq_lens,
+                                       int32_t max_seq_len, float softmax_scale,
+                                       const float* k_smooth, int32_t num_splits,
+                                       void* workspace, size_t workspace_bytes, void* out,
+                                       float* lse, void* stream) {
+  return decode_call(pool, q, batch, num_q_heads, block_table, max_pages, seq_lens, max_seq_len,
+                     softmax_scale, k_smooth, num_splits, workspace, workspace_bytes, out, lse,
+                     stream, true);
 }
 
 pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, int32_t batch,
@@ -204,6 +245,8 @@ pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, in
   if (batch == 0) return PKV_OK;
   if (!q || !block_table || !seq_lens || !out) return PKV_ERR_INVALID;
   if (pool->dtype == PKV_BF16 && k_smooth) return PKV_ERR_INVALID;
+  if (num_splits > 1 && (long long)batch * pool->num_kv_heads > kDecodeCounters)
+    return PKV_ERR_INVALID;
   const size_t cap = pkv_host::decode_fixed_scratch_bytes();
   Plan p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, num_splits);
   if (p.ws_bytes > cap) {
@@ -236,10 +279,7 @@ pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, in
   a.k_smooth = k_smooth;
   a.splits = p.splits;
   a.pages_per_split = p.pages_per_split;
-  a.ws_o = p.ws_bytes ? static_cast<float*>(scratch) : nullptr;
-  a.ws_lse = p.ws_bytes
-                 ? reinterpret_cast<float*>(static_cast<char*>(scratch) + p.ws_lse_offset)
-                 : nullptr;
+  set_workspace(a, p, scratch, false);
   a.out = out;
   a.lse = lse;
   return cuda_status(pkv_host::launch_decode(a, pool->dtype == PKV_INT8,

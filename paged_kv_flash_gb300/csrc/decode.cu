@@ -226,7 +226,10 @@ __device__ __forceinline__ void process_page(WarpState<G, INT8>& st, const uint8
   }
 }
 
-template <int G, bool INT8>
+// FUSED: the split that completes a (sequence, KV head) merges its splits
+// (a.ws_ctr counts them); otherwise a separate combine kernel does.  A
+// template parameter, so that the default kernel carries none of that code.
+template <int G, bool INT8, bool FUSED>
 __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
     decode_split_kernel(const __grid_constant__ pkv_host::DecodeLaunch a) {
   using C = Cfg<G, INT8>;
@@ -248,7 +251,10 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
   }
   const int npages = (L + kPageSize - 1) / kPageSize;
   const int p_begin = split * a.pages_per_split;
-  if (split > 0 && p_begin >= npages) return;   // empty split: the combine skips it
+  if (split > 0 && p_begin >= npages) return;   // empty split: the merge skips it
+  // splits holding keys (split 0 always runs); with one, it writes the output
+  const int nv = max(1, (npages + a.pages_per_split - 1) / a.pages_per_split);
+  const bool direct = a.splits == 1 || nv == 1;
   const int p_end = min(npages, p_begin + a.pages_per_split);
   const int n_w = max(0, (p_end - p_begin - warp + W - 1) / W);   // pages of this warp
 
@@ -460,7 +466,7 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
     }
     const float lse2 = (M == -INFINITY) ? -INFINITY : M + fast_log2(Lsum);
     const int hq = h * G + g;
-    if (a.splits == 1) {
+    if (direct) {
       static_cast<__nv_bfloat16*>(a.out)[((size_t)b * Hq + hq) * kHeadDim + d] =
           __float2bfloat16_rn(O);
       if (a.lse && d == 0) a.lse[(size_t)b * Hq + hq] = lse2 * kLn2;
@@ -470,10 +476,54 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
       if (d == 0) a.ws_lse[row] = lse2;
     }
   }
+  if (direct || !FUSED) return;                 // separate combine kernel
+
+  // Fused merge: count this split's part; the split that completes the count merges the
+  // nv parts of (b, KV head) (log-sum-exp rule, splits in order, so the
+  // result does not depend on which split merges) and resets the count.
+  // the flag sits in the unused end of the barrier header (no static shared
+  // memory: it would pad the 1024-byte aligned dynamic allocation)
+  volatile uint32_t& s_last = *reinterpret_cast<volatile uint32_t*>(smem + 1020);
+  static_assert(pkv_host::kDecodeWarps * 5 * 8 <= 1020, "barrier header");
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t* ctr = a.ws_ctr + (size_t)b * a.num_kv_heads + h;
+    uint32_t old;
+    asm volatile("fence.acq_rel.gpu;\n\tatom.relaxed.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(old) : "l"(ctr) : "memory");
+    const bool last = old == (uint32_t)(nv - 1);
+    if (last) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      *ctr = 0u;                                  // ready for the next call
+    }
+    s_last = last ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  for (int t = threadIdx.x; t < G * kHeadDim; t += W * 32) {
+    const int g = t / kHeadDim, d = t % kHeadDim;
+    const size_t bh = (size_t)b * Hq + h * G + g;
+    const float* lp = a.ws_lse + bh * a.splits;
+    const float* op = a.ws_o + bh * a.splits * kHeadDim;
+    float M = -INFINITY;
+    for (int sp = 0; sp < nv; ++sp) M = fmaxf(M, __ldcg(lp + sp));
+    float sum = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int sp = 0; sp < nv; ++sp) {
+        const float f = fast_exp2(__ldcg(lp + sp) - M);
+        sum += f;
+        O += f * __ldcg(op + (size_t)sp * kHeadDim + d);
+      }
+      O = O / sum;
+    }
+    static_cast<__nv_bfloat16*>(a.out)[bh * kHeadDim + d] = __float2bfloat16_rn(O);
+    if (a.lse && d == 0) a.lse[bh] = (M == -INFINITY) ? -INFINITY : (M + fast_log2(sum)) * kLn2;
+  }
 }
 
-// Combine: out = sum_s 2^(lse_s - lse) * O_s, lse = log2 sum_s 2^lse_s, over
-// the splits that hold keys (ceil(pages / pages_per_split) of them).
+// Combine (separate kernel): out = sum_s 2^(lse_s - lse) * O_s, lse = log2
+// sum_s 2^lse_s, over the splits that hold keys (ceil(pages / pages_per_split)
+// of them); rows whose keys fit one split were finished by that split.
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__
                                                              pkv_host::DecodeLaunch a) {
   const int bh = blockIdx.x;
@@ -483,6 +533,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   if (L < 0 || L > a.max_pages * kPageSize) L = 0;
   const int npages = (L + kPageSize - 1) / kPageSize;
   const int n = min(a.splits, (npages + a.pages_per_split - 1) / a.pages_per_split);
+  if (n <= 1) return;                           // one split: it wrote the output itself
   const float* lp = a.ws_lse + (size_t)bh * a.splits;
   const float* op = a.ws_o + (size_t)bh * a.splits * kHeadDim;
   float M = -INFINITY;
@@ -501,20 +552,25 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
     a.lse[bh] = (M == -INFINITY) ? -INFINITY : (M + fast_log2(sum)) * kLn2;
 }
 
-template <int G, bool INT8>
-cudaError_t launch_split(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
+template <int G, bool INT8, bool FUSED>
+cudaError_t launch_split_as(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
   using C = Cfg<G, INT8>;
   constexpr int smem = 1024 + pkv_host::kDecodeWarps * C::NBUF * C::BUF;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, INT8>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, INT8, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   dim3 grid(a.splits, a.num_kv_heads, a.batch);
-  decode_split_kernel<G, INT8><<<grid, pkv_host::kDecodeWarps * 32, smem, s>>>(a);
+  decode_split_kernel<G, INT8, FUSED><<<grid, pkv_host::kDecodeWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int G, bool INT8>
+cudaError_t launch_split(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
+  return a.ws_ctr ? launch_split_as<G, INT8, true>(a, s) : launch_split_as<G, INT8, false>(a, s);
 }
 
 template <bool INT8>
@@ -537,12 +593,9 @@ bool decode_supports_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8;
 cudaError_t launch_decode(const DecodeLaunch& a, bool int8, cudaStream_t s) {
   if (a.batch == 0) return cudaSuccess;
   cudaError_t e = int8 ? dispatch_group<true>(a, s) : dispatch_group<false>(a, s);
-  if (e != cudaSuccess) return e;
-  if (a.splits > 1) {
-    decode_combine_kernel<<<a.batch * a.num_q_heads, 128, 0, s>>>(a);
-    e = cudaGetLastError();
-  }
-  return e;
+  if (e != cudaSuccess || a.splits == 1 || a.ws_ctr) return e;
+  decode_combine_kernel<<<a.batch * a.num_q_heads, 128, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 uint32_t take_decode_error(cudaStream_t s) {

@@ -42,6 +42,8 @@ struct DecodeLaunch {
   float softmax_scale;
   const float* k_smooth;
   int splits, pages_per_split;
+  uint32_t* ws_ctr;        // fused merge: parts counted per b * Hkv + h (zero between
+                           // calls); null: a separate combine kernel merges
   float* ws_o;             // [B][Hq][splits][128] when splits > 1
   float* ws_lse;           // [B][Hq][splits]
   void* out;               // bf16 [B][Hq][128]

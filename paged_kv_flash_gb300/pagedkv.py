@@ -44,9 +44,11 @@ _POOLP = ctypes.POINTER(_Pool)
 SIGNATURES = {
     "pkv_kv_append": (_I, [_POOLP, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P]),
     "pkv_decode_plan": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
-                             ctypes.POINTER(_SZ)]),
+                             ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "pkv_paged_attn_decode": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P, _SZ,
                                    _P, _P, _P]),
+    "pkv_paged_attn_decode_fused": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P,
+                                         _SZ, _P, _P, _P]),
     "pkv_paged_attn_decode_noalloc": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P,
                                            _P, _P]),
     "pkv_prefill_plan": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
@@ -155,36 +157,50 @@ def kv_append(pool: Pool, k_new, v_new, cu_new, block_table, seq_lens, k_smooth=
 
 
 def decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits=0):
-    """(splits, pages_per_split, workspace_bytes) of a decode call."""
-    s, c, w = _I(), _I(), _SZ()
+    """(splits, pages_per_split, workspace_bytes, zero_bytes) of a decode call."""
+    s, c, w, z = _I(), _I(), _SZ(), _SZ()
     st = _lib.pkv_decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits,
-                              ctypes.byref(s), ctypes.byref(c), ctypes.byref(w))
+                              ctypes.byref(s), ctypes.byref(c), ctypes.byref(w), ctypes.byref(z))
     _check(st, "pkv_decode_plan")
-    return s.value, c.value, w.value
+    return s.value, c.value, w.value, z.value
+
+
+def decode_workspace(nbytes, zero_bytes, device="cuda"):
+    """A decode workspace of nbytes (at least 256) ready for its first call:
+    the leading zero_bytes (part counters) zeroed.  Calls leave it ready
+    again, so it is meant to be kept and reused."""
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    if zero_bytes:
+        ws[:zero_bytes].zero_()
+    return ws
 
 
 def paged_attn_decode(pool: Pool, q, block_table, seq_lens, max_seq_len, softmax_scale,
                       k_smooth=None, num_splits=0, workspace=None, out=None, lse=None,
-                      want_lse=True, stream=None):
-    """One query token per sequence: q [B][Hq][128] bf16 -> (out bf16, lse fp32)."""
+                      want_lse=True, stream=None, fused=False):
+    """One query token per sequence: q [B][Hq][128] bf16 -> (out bf16, lse fp32).
+    fused=True merges the splits inside the split kernel
+    (pkv_paged_attn_decode_fused; its workspace's counters must start zeroed,
+    as decode_workspace() leaves them)."""
     _need(q, torch.bfloat16, "q")
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
     B, Hq, _ = q.shape
-    _, _, ws_bytes = decode_plan(B, Hq, pool.num_kv_heads, max_seq_len, num_splits)
+    _, _, ws_bytes, zero_bytes = decode_plan(B, Hq, pool.num_kv_heads, max_seq_len, num_splits)
     if workspace is None and ws_bytes:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+        workspace = decode_workspace(ws_bytes, zero_bytes, q.device)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     pc = pool.c()
-    st = _lib.pkv_paged_attn_decode(
+    fn = _lib.pkv_paged_attn_decode_fused if fused else _lib.pkv_paged_attn_decode
+    st = fn(
         ctypes.byref(pc), _ptr(q), B, Hq, _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), int(max_seq_len), float(softmax_scale), _ptr(k_smooth),
         int(num_splits), _ptr(workspace), workspace.numel() if workspace is not None else 0,
         _ptr(out), _ptr(lse), _stream(stream))
-    _check(st, "pkv_paged_attn_decode")
+    _check(st, "pkv_paged_attn_decode_fused" if fused else "pkv_paged_attn_decode")
     return out, lse
 
 

@@ -93,12 +93,24 @@ def test_decode_rejects_bad_arguments(lib, bad):
 def test_decode_rejects_short_workspace(lib):
     # four splits of one page each need a workspace; none given
     assert decode(lib, good_pool(), splits=4) == INVALID
-    s, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    s, c, w, z = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
     assert lib.pkv_decode_plan(1, 4, 2, 64, 4, ctypes.byref(s), ctypes.byref(c),
-                               ctypes.byref(w)) == 0
+                               ctypes.byref(w), ctypes.byref(z)) == 0
     assert (s.value, c.value) == (4, 1) and w.value > 0
+    assert z.value == 65536 * 4                 # fixed counter region
     assert decode(lib, good_pool(), splits=4, ws=FAKE, ws_bytes=w.value - 1) == INVALID
     assert decode(lib, good_pool(), splits=4, ws=FAKE + 16, ws_bytes=w.value) == INVALID
+
+
+def test_forced_split_beyond_counter_region_is_rejected(lib):
+    s, c, w, z = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
+    # 8,193 sequences x 8 KV heads > 65,536 counters
+    assert lib.pkv_decode_plan(8193, 32, 8, 4096, 4, ctypes.byref(s), ctypes.byref(c),
+                               ctypes.byref(w), ctypes.byref(z)) == INVALID
+    # the heuristic does not split them
+    assert lib.pkv_decode_plan(8193, 32, 8, 4096, 0, ctypes.byref(s), ctypes.byref(c),
+                               ctypes.byref(w), ctypes.byref(z)) == 0
+    assert s.value == 1 and w.value == 0 and z.value == 0
 
 
 def test_decode_unsupported_group_size(lib):
@@ -110,16 +122,17 @@ def test_decode_empty_batch_is_a_no_op(lib):
 
 
 def test_plan_heuristic_bounds(lib):
-    s, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    s, c, w, z = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
     for B, Hkv, L in [(1, 8, 1024), (64, 8, 8192), (1, 8, 32768), (8, 8, 32768), (32, 8, 16398)]:
         assert lib.pkv_decode_plan(B, 4 * Hkv, Hkv, L, 0, ctypes.byref(s), ctypes.byref(c),
-                                   ctypes.byref(w)) == 0
+                                   ctypes.byref(w), ctypes.byref(z)) == 0
         pages = (L + 15) // 16
         assert 1 <= c.value <= 128 and s.value == -(-pages // c.value)
         if s.value > 1:
-            assert w.value >= B * 4 * Hkv * s.value * 129 * 4
+            assert z.value == 65536 * 4
+            assert w.value >= z.value + B * 4 * Hkv * s.value * 129 * 4
         else:
-            assert w.value == 0
+            assert w.value == 0 and z.value == 0
 
 
 def test_append_rejects_bad_arguments(lib):

@@ -168,3 +168,39 @@ def test_int8_group_sizes_ragged(pk, G):
         out, lse = gpu_decode(pk, case, splits, int8_pools=pools, smooth=w)
         check_out(out, ro, f"int8 G={G}")
         check_lse(lse, rl, f"int8 G={G}")
+
+
+def test_fused_decode_workspace_reuse_is_exact():
+    """The fused-merge decode: one workspace over a series of split calls
+    gives the same bits as a fresh workspace per call and as the separate
+    combine, and its part counters are zero after each call (the split that
+    completes the count merges and resets it)."""
+    from paged_kv_flash_gb300 import pagedkv as pk
+    rng = np.random.default_rng(77)
+    calls = []
+    # batch 2, then 4, then 3: a later call may need more counters than an
+    # earlier one wrote partials next to
+    for lens in ([1, 4000], [3000, 17, 700, 2048], [5000, 5000, 5000]):
+        case = W.decode_bf16(rng, np.array(lens, np.int32), 32, 8)
+        pool = pk.Pool(dev_bf16(case.k_pool), dev_bf16(case.v_pool))
+        args = (pool, dev_bf16(case.q), dev(case.layout.block_table), dev(case.seq_lens),
+                int(max(lens)), case.scale)
+        fresh = pk.paged_attn_decode(*args, num_splits=8, fused=True)
+        assert pk.poll_device_error() == pk.OK
+        sep = pk.paged_attn_decode(*args, num_splits=8)
+        assert torch.equal(fresh[0], sep[0]) and torch.equal(fresh[1], sep[1])
+        ro, rl = oracle.paged_attention(case.k_pool, case.v_pool, case.q,
+                                        W.cu_from_counts([1] * len(lens)),
+                                        case.layout.block_table, case.seq_lens, case.scale)
+        check_out(fresh[0], ro, f"fused decode {lens}")
+        check_lse(fresh[1], rl, f"fused decode {lens}")
+        calls.append((args, fresh))
+    plans = [pk.decode_plan(len(a[1]), 32, 8, a[4], 8) for a, _ in calls]
+    ws = pk.decode_workspace(max(p[2] for p in plans), max(p[3] for p in plans))
+    zero = max(p[3] for p in plans)
+    for _ in range(2):
+        for args, (o0, l0) in calls:
+            o, l = pk.paged_attn_decode(*args, num_splits=8, workspace=ws, fused=True)
+            assert torch.equal(o, o0) and torch.equal(l, l0)
+            assert int(ws[:zero].count_nonzero()) == 0
+    assert pk.poll_device_error() == pk.OK
