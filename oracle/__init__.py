@@ -53,6 +53,11 @@ def _load():
         lib.orc_kv_append_int8.restype = I
         lib.orc_quantize_row_int8.argtypes = [P, P, I, P, P]
         lib.orc_quantize_row_int8.restype = None
+        lib.orc_qkv_norm_rope_append.argtypes = [P, I, I, I, P, P, ctypes.c_double, P, P, I, P,
+                                                 I, P, I, P, P, P, P, I, I]
+        lib.orc_qkv_norm_rope_append.restype = I
+        lib.orc_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.orc_bf16_from_double.restype = ctypes.c_uint16
         _lib = lib
     return _lib
 
@@ -154,3 +159,36 @@ def quantize_row_int8(x_bits, w=None):
     scale = np.zeros(1, np.float32)
     lib.orc_quantize_row_int8(_ptr(x), _ptr(w), x.shape[0], _ptr(codes), _ptr(scale))
     return codes, scale[0]
+
+
+def bf16_from_double(v):
+    """v rounded to the nearest bf16 (ties to even), as uint16 bits."""
+    return int(_load().orc_bf16_from_double(float(v)))
+
+
+def qkv_norm_rope_append(qkv, Hq, Hkv, q_w, k_w, eps, cos_tab, sin_tab, cu_new, block_table,
+                         seq_lens, k_pool, v_pool):
+    """Fused attention inputs: qkv uint16 bf16 bits [T][Hq + 2 Hkv][D] -> q_out
+    bits [T][Hq][D] and copies of the bf16 pools with the new tokens' K
+    (normed, rotated) and V written.  q_w / k_w: fp32 [D] or None (no norm);
+    cos_tab / sin_tab: fp32 [max_pos][D/2] or None (no RoPE)."""
+    lib = _load()
+    qkv = _c(qkv, np.uint16)
+    T, H, D = qkv.shape
+    assert H == Hq + 2 * Hkv
+    k_pool = np.array(k_pool, dtype=np.uint16, copy=True)
+    v_pool = np.array(v_pool, dtype=np.uint16, copy=True)
+    num_pages, hkv_pool, P, Dp = k_pool.shape
+    assert hkv_pool == Hkv and Dp == D
+    qw, kw = _c(q_w, np.float32), _c(k_w, np.float32)
+    ct, st = _c(cos_tab, np.float32), _c(sin_tab, np.float32)
+    max_pos = 0 if ct is None else ct.shape[0]
+    cu_new, bt, sl = _c(cu_new, np.int32), _c(block_table, np.int32), _c(seq_lens, np.int32)
+    q_out = np.zeros((T, Hq, D), np.uint16)
+    rc = lib.orc_qkv_norm_rope_append(_ptr(qkv), Hq, Hkv, D, _ptr(qw), _ptr(kw), float(eps),
+                                      _ptr(ct), _ptr(st), max_pos, _ptr(cu_new), sl.shape[0],
+                                      _ptr(bt), bt.shape[1], _ptr(sl), _ptr(q_out),
+                                      _ptr(k_pool), _ptr(v_pool), num_pages, P)
+    if rc != 0:
+        raise ValueError("oracle: position outside the block table or the RoPE table")
+    return q_out, k_pool, v_pool

@@ -28,6 +28,9 @@
  *  - The KV write copies the new K/V vectors into the pages named by the
  *    block table (same page, list of fused kernels, "the KV cache write").
  *    orc_kv_append_bf16.
+ *  - The fused attention-input step (same list: q/k RMSNorm, RoPE and the KV
+ *    cache write from the fused q/k/v projection) is restated, with its
+ *    readings, above orc_qkv_norm_rope_append.
  *
  * Readings where the pages are silent:
  *  - Causal alignment is bottom-right: query row i of a sequence with q_b new
@@ -403,3 +406,110 @@ int orc_kv_append_int8(int8_t* pool_k, int8_t* pool_v, float* k_scale, float* v_
   }
   return 0;
 }
+
+/* ------------------------------------------------ fused attention inputs */
+
+/*
+ * The "attention inputs" fused kernel of the same page's list of fused
+ * kernels: from the fused q/k/v projection output, q/k RMSNorm, RoPE and the
+ * KV cache write, bit-identical to the chain it replaces (3 copies, 2 norms,
+ * 2 RoPE, 1 write).  The pages give no formulas; readings (stated once here
+ * and in the build's notes):
+ *  - RMSNorm over one head's D channels: r = 1 / sqrt(mean_c x_c^2 + eps),
+ *    n_c = bf16(x_c * r * w_c); the chain's norm kernel writes bf16.  A NULL
+ *    weight means that part has no norm (n = x).
+ *  - RoPE by halves (channel i pairs with i + D/2, i < D/2) at the token's
+ *    position p, with cos/sin from a caller table [max_pos][D/2]:
+ *    o_i = bf16(n_i cos - n_{i+D/2} sin), o_{i+D/2} = bf16(n_{i+D/2} cos +
+ *    n_i sin).  A NULL table means no RoPE (o = n).
+ *  - q heads go to q_out [T][Hq][D]; k heads, normed and rotated, and v
+ *    heads, copied, go to the pool slots of the new tokens (positions as in
+ *    orc_kv_append_bf16).  The projection output is [T][Hq + 2 Hkv][D]: q
+ *    heads, then k heads, then v heads.
+ * Every product and sum is fp64 (bf16 and fp32 inputs are exact there); the
+ * result is rounded to bf16 (round to nearest, ties to even) exactly where
+ * the chain stores bf16.
+ */
+
+/* v rounded to the nearest bf16 (ties to even), as raw bits. */
+static uint16_t bf16_bits_from_double(double v) {
+  if (isnan(v)) return 0x7FC0;
+  const uint16_t sign = signbit(v) ? 0x8000 : 0;
+  const double a = fabs(v);
+  if (a == 0.0) return sign;
+  int e;
+  const double m = frexp(a, &e);                /* a = m 2^e, m in [1/2, 1) */
+  /* 8 significant bits for normals (2^-126 <= a), fewer below */
+  int bits = 8;
+  if (e < -125) bits = 8 - (-125 - e);
+  const double r = ldexp(nearbyint(ldexp(m, bits)), e - bits);
+  if (r >= 0x1.0p128) return sign | 0x7F80;     /* rounds past the largest finite */
+  const float f = (float)r;                     /* exact: r is a bf16 value */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return sign | (uint16_t)(u >> 16);
+}
+
+/* RMSNorm (if w) then RoPE (if cos_row) of one head vector of D bf16 values. */
+static void norm_rope(const uint16_t* x, int D, const float* w, double eps, const float* cos_row,
+                      const float* sin_row, uint16_t* out) {
+  uint16_t n[1024];
+  if (w) {
+    double ss = 0.0;
+    for (int c = 0; c < D; ++c) {
+      const double v = bf16_bits_to_double(x[c]);
+      ss += v * v;
+    }
+    const double r = 1.0 / sqrt(ss / D + eps);
+    for (int c = 0; c < D; ++c) n[c] = bf16_bits_from_double(bf16_bits_to_double(x[c]) * r * w[c]);
+  } else {
+    memcpy(n, x, sizeof(uint16_t) * (size_t)D);
+  }
+  if (cos_row) {
+    const int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+      const double a = bf16_bits_to_double(n[i]), b = bf16_bits_to_double(n[i + half]);
+      const double c = cos_row[i], s = sin_row[i];
+      out[i] = bf16_bits_from_double(a * c - b * s);
+      out[i + half] = bf16_bits_from_double(b * c + a * s);
+    }
+  } else {
+    memcpy(out, n, sizeof(uint16_t) * (size_t)D);
+  }
+}
+
+int orc_qkv_norm_rope_append(const uint16_t* qkv, int Hq, int Hkv, int D, const float* q_w,
+                             const float* k_w, double eps, const float* cos_tab,
+                             const float* sin_tab, int max_pos, const int32_t* cu_new, int B,
+                             const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                             uint16_t* q_out, uint16_t* pool_k, uint16_t* pool_v, int num_pages,
+                             int page_size) {
+  if (D <= 0 || D > 1024 || D % 2) return -1;
+  const int H = Hq + 2 * Hkv;
+  for (int b = 0; b < B; ++b) {
+    const int n = cu_new[b + 1] - cu_new[b];
+    for (int i = 0; i < n; ++i) {
+      const int p = seq_lens[b] - n + i;
+      const long fs = new_token_slot(block_table, max_pages, page_size, cu_new, seq_lens, b, i);
+      if (fs < 0) return -1;
+      if (cos_tab && (p < 0 || p >= max_pos)) return -1;
+      const long page = fs / page_size, slot = fs % page_size;
+      if (page < 0 || page >= num_pages) return -1;
+      const int t = cu_new[b] + i;
+      const float* cr = cos_tab ? cos_tab + (size_t)p * (D / 2) : NULL;
+      const float* sr = sin_tab ? sin_tab + (size_t)p * (D / 2) : NULL;
+      const uint16_t* row = qkv + (size_t)t * H * D;
+      for (int h = 0; h < Hq; ++h)
+        norm_rope(row + (size_t)h * D, D, q_w, eps, cr, sr, q_out + ((size_t)t * Hq + h) * D);
+      for (int h = 0; h < Hkv; ++h) {
+        const size_t dst = ((size_t)(page * Hkv + h) * page_size + slot) * D;
+        norm_rope(row + (size_t)(Hq + h) * D, D, k_w, eps, cr, sr, pool_k + dst);
+        memcpy(pool_v + dst, row + (size_t)(Hq + Hkv + h) * D, sizeof(uint16_t) * (size_t)D);
+      }
+    }
+  }
+  return 0;
+}
+
+/* Exposed for the pins: v rounded to bf16 bits. */
+uint16_t orc_bf16_from_double(double v) { return bf16_bits_from_double(v); }

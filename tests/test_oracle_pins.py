@@ -392,3 +392,161 @@ def test_int8_append_rows_are_quantised_rows():
             assert np.array_equal(v8[page, h, p % P], cv) and vs[page, h, p % P] == sv
             touched[page, h, p % P] = True
     assert np.all(np.isnan(ks[~touched])) and np.all(k8[~touched] == 0x5A)
+
+
+# ------------------------------------------------ fused attention inputs
+
+def _bits(vals):
+    return np.asarray(W.to_bf16_bits(np.asarray(vals, np.float32)), np.uint16).reshape(-1)
+
+
+def _one_token_case(D, x, Hq=1, Hkv=1):
+    """One token of one sequence at position 0: qkv rows q = x, k = x, v = x."""
+    qkv = np.stack([np.stack([x] * (Hq + 2 * Hkv))])            # [1][H][D]
+    kp = np.full((2, Hkv, P, D), W.BF16_NAN, np.uint16)
+    vp = kp.copy()
+    return qkv, kp, vp, np.array([0, 1], np.int32), np.array([[1]], np.int32), \
+        np.array([1], np.int32)
+
+
+def test_bf16_rounding_ties_to_even_and_subnormals():
+    assert oracle.bf16_from_double(1.0) == 0x3F80
+    assert oracle.bf16_from_double(1 + 2 ** -8) == 0x3F80        # tie -> even
+    assert oracle.bf16_from_double(1 + 3 * 2 ** -8) == 0x3F82    # tie -> even
+    assert oracle.bf16_from_double(1 + 2 ** -8 + 2 ** -30) == 0x3F81
+    assert oracle.bf16_from_double(-2.5) == 0xC020
+    assert oracle.bf16_from_double(2 ** -133) == 0x0001          # smallest subnormal
+    assert oracle.bf16_from_double(3.4e38) == 0x7F80             # past the largest finite
+    # against torch's bf16 conversion on a spread of exactly-fp32 values
+    rng = np.random.default_rng(11)
+    v = (rng.standard_normal(4000) * np.exp2(rng.integers(-40, 40, 4000))).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    got = np.array([oracle.bf16_from_double(float(t)) for t in v], np.uint16)
+    assert np.array_equal(got, ref)
+    # around the smallest normal (2^-126) and through the subnormals
+    v = (rng.uniform(1.0, 2.0, 2000) * np.exp2(rng.integers(-134, -120, 2000))).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    got = np.array([oracle.bf16_from_double(float(t)) for t in v], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def _golden_rows():
+    with open(os.path.join(GOLDEN, "qkv_norm_rope_d4.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = [np.array([float(t) for t in p.split()]) for p in line.split("|")]
+            yield parts
+
+
+@pytest.mark.parametrize("row", list(range(3)))
+def test_norm_rope_golden_d4(row):
+    x, w, c, s, want = list(_golden_rows())[row]
+    D = 4
+    qkv, kp, vp, cu, bt, sl = _one_token_case(D, _bits(x))
+    q, k, v = oracle.qkv_norm_rope_append(qkv, 1, 1, w.astype(np.float32), w.astype(np.float32),
+                                          0.0, c[None].astype(np.float32),
+                                          s[None].astype(np.float32), cu, bt, sl, kp, vp)
+    assert np.array_equal(q[0, 0], _bits(want))
+    assert np.array_equal(k[bt[0, 0], 0, 0], _bits(want))       # K gets the same steps
+    assert np.array_equal(v[bt[0, 0], 0, 0], _bits(x))          # V is copied
+
+
+def test_no_norm_no_rope_is_the_plain_append():
+    rng = np.random.default_rng(12)
+    Hq, Hkv = 4, 2
+    lens, news = np.array([37, 5], np.int32), np.array([7, 5], np.int32)
+    lay = W.scatter_pages(rng, lens)
+    T = int(news.sum())
+    qkv = W.normal_bf16(rng, (T, Hq + 2 * Hkv, D))
+    kp, vp = W.empty_pool_bf16(lay.num_pages, Hkv)
+    cu = W.cu_from_counts(news)
+    q, k, v = oracle.qkv_norm_rope_append(qkv, Hq, Hkv, None, None, 0.0, None, None, cu,
+                                          lay.block_table, lens, kp, vp)
+    assert np.array_equal(q, qkv[:, :Hq])
+    k2, v2 = oracle.kv_append_bf16(kp, vp, qkv[:, Hq:Hq + Hkv], qkv[:, Hq + Hkv:], cu,
+                                   lay.block_table, lens)
+    assert np.array_equal(k, k2) and np.array_equal(v, v2)
+
+
+def test_rmsnorm_is_scale_free_and_unit_rms():
+    rng = np.random.default_rng(13)
+    x = W.normal_bf16(rng, (D,))
+    x2 = _bits(2.0 * W.bits_to_float(x))                        # exact doubling
+    ones = np.ones(D, np.float32)
+    outs = []
+    for xx in (x, x2):
+        qkv, kp, vp, cu, bt, sl = _one_token_case(D, xx)
+        q, _, _ = oracle.qkv_norm_rope_append(qkv, 1, 1, ones, ones, 0.0, None, None, cu, bt,
+                                              sl, kp, vp)
+        outs.append(q[0, 0])
+    assert np.array_equal(outs[0], outs[1])
+    n = W.bits_to_float(outs[0]).astype(np.float64)
+    assert abs(np.mean(n * n) - 1.0) < 4 * 2.0 ** -8             # unit RMS up to bf16 rounding
+    # the weight multiplies channel by channel
+    w = rng.uniform(0.5, 2.0, D).astype(np.float32)
+    qkv, kp, vp, cu, bt, sl = _one_token_case(D, x)
+    qw, _, _ = oracle.qkv_norm_rope_append(qkv, 1, 1, w, w, 0.0, None, None, cu, bt, sl, kp, vp)
+    assert np.allclose(W.bits_to_float(qw[0, 0]), n * w, rtol=2 * 2.0 ** -8, atol=0)
+
+
+def _rope_table(max_pos, base=1.0e6):
+    inv = base ** (-np.arange(0, D, 2, dtype=np.float64) / D)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+def test_rope_rotates_pairs_and_keeps_relative_position():
+    rng = np.random.default_rng(14)
+    cos_t, sin_t = _rope_table(64)
+    q0, k0 = W.normal_bf16(rng, (D,)), W.normal_bf16(rng, (D,))
+
+    def rot(x, p):
+        qkv, kp, vp, _, bt, _ = _one_token_case(D, x)
+        sl = np.array([p + 1], np.int32)
+        bt = np.zeros((1, 8), np.int32)
+        bt[0, p // P] = 1
+        q, _, _ = oracle.qkv_norm_rope_append(qkv, 1, 1, None, None, 0.0, cos_t, sin_t,
+                                              np.array([0, 1], np.int32), bt, sl, kp, vp)
+        return W.bits_to_float(q[0, 0]).astype(np.float64)
+
+    # position 0 is the identity
+    assert np.array_equal(rot(q0, 0), W.bits_to_float(q0).astype(np.float64))
+    # each (i, i + D/2) pair keeps its length
+    x = W.bits_to_float(q0).astype(np.float64)
+    r = rot(q0, 37)
+    half = D // 2
+    assert np.allclose(np.hypot(r[:half], r[half:]), np.hypot(x[:half], x[half:]),
+                       rtol=3 * 2.0 ** -8, atol=1e-6)
+    # <rot(q, m), rot(k, n)> depends only on m - n
+    dots = [rot(q0, m) @ rot(k0, m - 5) for m in (5, 20, 50)]
+    assert np.allclose(dots, dots[0], rtol=0, atol=0.05 * np.sqrt(D))
+    # ... and does change with m - n
+    assert abs(rot(q0, 40) @ rot(k0, 0) - dots[0]) > 0.05 * np.sqrt(D)
+
+
+def test_rope_quarter_turn_swaps_halves_exactly():
+    rng = np.random.default_rng(15)
+    x = W.normal_bf16(rng, (D,))
+    cos_t = np.zeros((1, D // 2), np.float32)
+    sin_t = np.ones((1, D // 2), np.float32)
+    qkv, kp, vp, cu, bt, sl = _one_token_case(D, x)
+    q, _, _ = oracle.qkv_norm_rope_append(qkv, 1, 1, None, None, 0.0, cos_t, sin_t, cu, bt, sl,
+                                          kp, vp)
+    xf = W.bits_to_float(x)
+    half = D // 2
+    want = np.concatenate([-xf[half:], xf[:half]])
+    assert np.array_equal(W.bits_to_float(q[0, 0]), want)
+
+
+def test_q_and_k_take_their_own_weights():
+    rng = np.random.default_rng(16)
+    x = W.normal_bf16(rng, (D,))
+    qw = np.full(D, 1.0, np.float32)
+    kw = np.full(D, 0.5, np.float32)
+    qkv, kp, vp, cu, bt, sl = _one_token_case(D, x)
+    q, k, _ = oracle.qkv_norm_rope_append(qkv, 1, 1, qw, kw, 0.0, None, None, cu, bt, sl, kp, vp)
+    qf = W.bits_to_float(q[0, 0])
+    kf = W.bits_to_float(k[bt[0, 0], 0, 0])
+    assert np.array_equal(kf, qf * np.float32(0.5))      # halving is exact in bf16
