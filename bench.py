@@ -18,7 +18,8 @@ The JSON line reports the step time (value, us per step) and, from CUDA
 events around every call, decode HBM GB/s and prefill TFLOP/s; the roofline
 object is for the prefill kernel, which dominates the step.  "configs" holds
 the other workloads (single-sequence decode, 1,024-token prefill, batched
-decode, INT8 32k decode) timed with a 512 MB L2 flush between runs.
+decode, INT8 32k decode, the fused attention-input step on a 2,048-token
+chunk) timed with a 512 MB L2 flush between runs.
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 """
 import argparse
@@ -427,7 +428,34 @@ def other_configs(torch, pk, hbm, bf16):
         "graph_note": "back-to-back launches in one CUDA graph, warm L2",
         "append_us": round(a_med, 2), "append_GBps": round(2 * 2 * 1024 * 8 * 256 / a_med / 1e3, 1)}
     assert pk.poll_device_error() == pk.OK
+    del pool
+    # fused attention inputs for one 2,048-token chunk at positions 14,336..16,383
+    fn, byts = qkv_prep_fn(torch, pk, 95)
+    med, mn = time_events(torch, fn, flush=flush)
+    res["qkv_norm_rope_append_chunk2048"] = {
+        "us": round(med, 2), "us_min": round(mn, 2), "GBps": round(byts / med / 1e3, 1),
+        "frac_of_measured": round(byts / med / 1e3 / hbm, 4), "bytes": int(byts),
+        "note": ("q/k RMSNorm + RoPE + KV write from the q/k/v projection output, "
+                 "GQA 32/8; bytes = projection read + q_out, K, V writes + RoPE rows")}
+    assert pk.poll_device_error() == pk.OK
     return res
+
+
+def qkv_prep_fn(torch, pk, seed, T=2048, L=16384, Hq=32, Hkv=8):
+    """The fused attention-input call for T new tokens ending at position L,
+    and its algorithmic bytes (every input and output element once)."""
+    case = W.qkv_prep_case(seed, [T], [L], Hq=Hq, Hkv=Hkv)
+    pool = pk.Pool.empty(case.layout.num_pages, Hkv)
+    qkv = to_dev_bf16(torch, case.qkv)
+    tf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    qw, kw, cs, sn = tf(case.q_w), tf(case.k_w), tf(case.cos), tf(case.sin)
+    cu, bt, sl = (to_dev(torch, case.cu_new), to_dev(torch, case.layout.block_table),
+                  to_dev(torch, case.seq_lens))
+    q_out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device="cuda")
+    fn = lambda: pk.qkv_norm_rope_append(pool, qkv, Hq, cu, bt, sl, q_norm_w=qw, k_norm_w=kw,
+                                         rope_cos=cs, rope_sin=sn, q_out=q_out)
+    byts = T * (Hq + 2 * Hkv) * D * 2 * 2 + T * D * 4
+    return fn, byts
 
 
 # ----------------------------------------------------- CPU baseline (oracle)
@@ -509,8 +537,8 @@ def cpu_baseline(mixed_wl, budget_s=20.0):
 
 def profile_case(torch, pk, name, reps=3):
     """One kernel on a fixed, seeded workload, launched `reps` times (for ncu
-    captures of a single launch: -k <kernel> -s 2 -c 1).  Prints the CUDA-event
-    time of an extra 10 launches."""
+    captures of a single launch: -k <kernel> -s 2 -c 1).  Prints the median
+    CUDA-event time of 10 more launches, each after an L2 flush."""
     rng = np.random.default_rng(5)
     if name == "prefill_chunk":
         qlen, L = 2048, 16384
@@ -551,18 +579,18 @@ def profile_case(torch, pk, name, reps=3):
                                           out=out, lse=lse)
         work = decode_bytes(case.seq_lens, case.Hkv, per)
         unit = "GB/s"
+    elif name == "qkv_prep":
+        fn, work = qkv_prep_fn(torch, pk, 95)
+        unit = "GB/s"
     else:
         raise SystemExit(f"unknown profile case {name}")
     for _ in range(reps):
         fn()
     torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(10):
-        fn()
-    e.record()
-    torch.cuda.synchronize()
-    us = s.elapsed_time(e) * 100.0
+    # per-launch time with a 512 MB L2 flush before each launch (back-to-back
+    # launches of a short kernel would time the Python call, not the kernel)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    us, _ = time_events(torch, fn, iters=10, warm=0, flush=flush)
     rate = work / us / (1e6 if unit == "TFLOP/s" else 1e3)
     assert pk.poll_device_error() == pk.OK
     print(json.dumps({"profile_case": name, "us": round(us, 2), unit: round(rate, 1)}))
@@ -578,7 +606,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill_chunk", "decode_bf16", "decode_int8"],
+    ap.add_argument("--profile-case", choices=["prefill_chunk", "decode_bf16", "decode_int8",
+                                                      "qkv_prep"],
                     help="run one kernel on a fixed workload (for ncu) and exit")
     args = ap.parse_args()
     K, Wu = args.steps, max(3, args.warmup)

@@ -256,6 +256,41 @@ pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, int32_t t
                                   void* out, float* lse, void* stream);
 
 /*
+ * qkv_norm_rope_append -- the fused attention-input step: from the fused
+ * q/k/v projection output, per-head RMSNorm of q and k, RoPE, and the KV
+ * cache write, in one kernel ("Fused kernels ...": the attention-input
+ * kernel that replaces 3 copies, 2 norms, 2 RoPE and 1 write, bit-identical
+ * to that chain).
+ *
+ *  qkv        bf16 [num_tokens][num_q_heads + 2 Hkv][128]: q heads, then k
+ *             heads, then v heads (16-byte aligned).
+ *  q_norm_w,  fp32 [128] RMSNorm weights of q and of k, or NULL for no norm
+ *  k_norm_w   on that part; eps > 0 typical (1e-6).  n_c = bf16(x_c * r *
+ *             w_c), r = 1 / sqrt(mean_c x_c^2 + eps), fp32 (r correctly
+ *             rounded).
+ *  rope_cos,  fp32 [max_pos][64] each, or both NULL for no RoPE.  Channel i
+ *  rope_sin   pairs with i + 64 at the token's position p: o_i = bf16(n_i
+ *             cos[p][i] - n_{i+64} sin[p][i]), o_{i+64} = bf16(n_{i+64}
+ *             cos[p][i] + n_i sin[p][i]), fp32, each product and sum
+ *             rounded once.
+ *  cu_new, block_table, max_pages, seq_lens: as pkv_kv_append; token i of
+ *             sequence b sits at position seq_lens[b] - n_b + i (p < max_pos
+ *             with RoPE).
+ *  q_out      bf16 [num_tokens][num_q_heads][128] (16-byte aligned).
+ * The k heads (normed and rotated) and the v heads (copied) go to the new
+ * tokens' pool slots.  bf16 pools only (PKV_ERR_UNSUPPORTED for INT8: append
+ * q_out's K through pkv_kv_append instead).  A token whose position or page
+ * falls outside the caller's arrays is skipped and flagged for
+ * pkv_poll_device_error.
+ */
+pkv_status pkv_qkv_norm_rope_append(const pkv_pool* pool, const void* qkv, int32_t num_tokens,
+                                    int32_t num_q_heads, const float* q_norm_w,
+                                    const float* k_norm_w, float eps, const float* rope_cos,
+                                    const float* rope_sin, int32_t max_pos, const int32_t* cu_new,
+                                    int32_t batch, const int32_t* block_table, int32_t max_pages,
+                                    const int32_t* seq_lens, void* q_out, void* stream);
+
+/*
  * Synchronises the stream, then reports and clears the device-side error
  * words of the kernels: PKV_ERR_TIMEOUT if a bounded wait ran out (its
  * outputs are garbage), else PKV_ERR_INVALID if a device-side check of the

@@ -414,21 +414,24 @@ int orc_kv_append_int8(int8_t* pool_k, int8_t* pool_v, float* k_scale, float* v_
  * kernels: from the fused q/k/v projection output, q/k RMSNorm, RoPE and the
  * KV cache write, bit-identical to the chain it replaces (3 copies, 2 norms,
  * 2 RoPE, 1 write).  The pages give no formulas; readings (stated once here
- * and in the build's notes):
- *  - RMSNorm over one head's D channels: r = 1 / sqrt(mean_c x_c^2 + eps),
- *    n_c = bf16(x_c * r * w_c); the chain's norm kernel writes bf16.  A NULL
+ * and in the build's notes), with the chain taken to be fp32 GPU kernels
+ * that store bf16:
+ *  - RMSNorm over one head's D channels: r = 1 / sqrt(mean_c x_c^2 + eps)
+ *    (mean in fp64, exact for bf16 inputs of ordinary range; r rounded to
+ *    fp32), n_c = bf16((x_c * r) * w_c) with both products in fp32.  A NULL
  *    weight means that part has no norm (n = x).
  *  - RoPE by halves (channel i pairs with i + D/2, i < D/2) at the token's
- *    position p, with cos/sin from a caller table [max_pos][D/2]:
- *    o_i = bf16(n_i cos - n_{i+D/2} sin), o_{i+D/2} = bf16(n_{i+D/2} cos +
- *    n_i sin).  A NULL table means no RoPE (o = n).
+ *    position p, with cos/sin from a caller table [max_pos][D/2], every
+ *    product and sum in fp32: o_i = bf16(n_i cos - n_{i+D/2} sin),
+ *    o_{i+D/2} = bf16(n_{i+D/2} cos + n_i sin).  A NULL table means no RoPE
+ *    (o = n).
  *  - q heads go to q_out [T][Hq][D]; k heads, normed and rotated, and v
  *    heads, copied, go to the pool slots of the new tokens (positions as in
  *    orc_kv_append_bf16).  The projection output is [T][Hq + 2 Hkv][D]: q
  *    heads, then k heads, then v heads.
- * Every product and sum is fp64 (bf16 and fp32 inputs are exact there); the
- * result is rounded to bf16 (round to nearest, ties to even) exactly where
- * the chain stores bf16.
+ * Rounding to bf16 is round to nearest, ties to even, exactly where the
+ * chain stores bf16.  (The file is built with -ffp-contract=off, so no
+ * product and sum below fuse into one rounding.)
  */
 
 /* v rounded to the nearest bf16 (ties to even), as raw bits. */
@@ -460,18 +463,24 @@ static void norm_rope(const uint16_t* x, int D, const float* w, double eps, cons
       const double v = bf16_bits_to_double(x[c]);
       ss += v * v;
     }
-    const double r = 1.0 / sqrt(ss / D + eps);
-    for (int c = 0; c < D; ++c) n[c] = bf16_bits_from_double(bf16_bits_to_double(x[c]) * r * w[c]);
+    const float r = (float)(1.0 / sqrt(ss / D + eps));
+    for (int c = 0; c < D; ++c) {
+      const float xr = bf16_bits_to_float(x[c]) * r;
+      const float y = xr * w[c];
+      n[c] = bf16_bits_from_double((double)y);
+    }
   } else {
     memcpy(n, x, sizeof(uint16_t) * (size_t)D);
   }
   if (cos_row) {
     const int half = D / 2;
     for (int i = 0; i < half; ++i) {
-      const double a = bf16_bits_to_double(n[i]), b = bf16_bits_to_double(n[i + half]);
-      const double c = cos_row[i], s = sin_row[i];
-      out[i] = bf16_bits_from_double(a * c - b * s);
-      out[i + half] = bf16_bits_from_double(b * c + a * s);
+      const float a = bf16_bits_to_float(n[i]), b = bf16_bits_to_float(n[i + half]);
+      const float c = cos_row[i], s = sin_row[i];
+      const float ac = a * c, bs = b * s, bc = b * c, as = a * s;
+      const float lo = ac - bs, hi = bc + as;
+      out[i] = bf16_bits_from_double((double)lo);
+      out[i + half] = bf16_bits_from_double((double)hi);
     }
   } else {
     memcpy(out, n, sizeof(uint16_t) * (size_t)D);

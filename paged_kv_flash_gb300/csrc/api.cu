@@ -323,11 +323,41 @@ pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, int32_t t
   return cuda_status(e);
 }
 
+pkv_status pkv_qkv_norm_rope_append(const pkv_pool* pool, const void* qkv, int32_t num_tokens,
+                                    int32_t num_q_heads, const float* q_norm_w,
+                                    const float* k_norm_w, float eps, const float* rope_cos,
+                                    const float* rope_sin, int32_t max_pos, const int32_t* cu_new,
+                                    int32_t batch, const int32_t* block_table, int32_t max_pages,
+                                    const int32_t* seq_lens, void* q_out, void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0 || batch < 0 || max_pages < 0 || num_q_heads <= 0 ||
+      num_q_heads % pool->num_kv_heads || !std::isfinite(eps) || eps < 0.f)
+    return PKV_ERR_INVALID;
+  if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (batch == 0 || max_pages == 0) return PKV_ERR_INVALID;
+  if (!qkv || !cu_new || !block_table || !seq_lens || !q_out) return PKV_ERR_INVALID;
+  if (!rope_cos != !rope_sin || (rope_cos && max_pos <= 0)) return PKV_ERR_INVALID;
+  if (!aligned(qkv, 16) || !aligned(q_out, 16)) return PKV_ERR_INVALID;
+  for (const void* p : {(const void*)q_norm_w, (const void*)k_norm_w, (const void*)rope_cos,
+                        (const void*)rope_sin})
+    if (p && !aligned(p, 16)) return PKV_ERR_INVALID;
+  if (num_tokens > 2147483647 / (num_q_heads + 2 * pool->num_kv_heads) / 64)
+    return PKV_ERR_UNSUPPORTED;
+  pkv_host::QkvPrepLaunch a{qkv,       num_tokens, num_q_heads,  pool->num_kv_heads,
+                            q_norm_w,  k_norm_w,   eps,          rope_cos,
+                            rope_sin,  max_pos,    cu_new,       batch,
+                            block_table, max_pages, seq_lens,    pool->k,
+                            pool->v,   pool->num_pages, q_out};
+  return cuda_status(pkv_host::launch_qkv_prep(a, static_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_poll_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
   const uint32_t e = pkv_host::take_append_error(s) | pkv_host::take_decode_error(s) |
-                     pkv_host::take_prefill_error(s);
+                     pkv_host::take_prefill_error(s) | pkv_host::take_qkv_error(s);
   if (e == ~0u) return PKV_ERR_CUDA;
   if (e & pkv::kErrTimeout) return PKV_ERR_TIMEOUT;
   return e ? PKV_ERR_INVALID : PKV_OK;

@@ -96,6 +96,29 @@ int prefill_ctas(int sms);
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s);
 uint32_t take_prefill_error(cudaStream_t s);
 
+struct QkvPrepLaunch {
+  const void* qkv;         // bf16 [T][Hq + 2 Hkv][128]
+  int num_tokens, num_q_heads, num_kv_heads;
+  const float* q_w;        // fp32 [128] or null
+  const float* k_w;
+  float eps;
+  const float* cos;        // fp32 [max_pos][64] or null
+  const float* sin;
+  int max_pos;
+  const int32_t* cu_new;   // [B+1]
+  int batch;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  void* k;                 // bf16 pool
+  void* v;
+  int num_pages;
+  void* q_out;             // bf16 [T][Hq][128]
+};
+
+cudaError_t launch_qkv_prep(const QkvPrepLaunch& a, cudaStream_t s);
+uint32_t take_qkv_error(cudaStream_t s);
+
 int sm_count();
 
 }  // namespace pkv_host

@@ -54,6 +54,8 @@ SIGNATURES = {
     "pkv_prefill_plan": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "pkv_paged_attn_prefill": (_I, [_POOLP, _P, _I, _P, _I, _I, _P, _I, _P, _I, _F, _P, _SZ, _P,
                                     _P, _P]),
+    "pkv_qkv_norm_rope_append": (_I, [_POOLP, _P, _I, _I, _P, _P, _F, _P, _P, _I, _P, _I, _P,
+                                      _I, _P, _P, _P]),
     "pkv_poll_device_error": (_I, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
     "pkv_device_sm_count": (_I, []),
@@ -268,6 +270,32 @@ def paged_attn_prefill(pool: Pool, q, cu_q, block_table, seq_lens, max_q_len, so
         _stream(stream))
     _check(st, "pkv_paged_attn_prefill")
     return out, lse
+
+
+def qkv_norm_rope_append(pool: Pool, qkv, num_q_heads, cu_new, block_table, seq_lens,
+                         q_norm_w=None, k_norm_w=None, eps=1e-6, rope_cos=None, rope_sin=None,
+                         q_out=None, stream=None):
+    """Fused attention inputs (see pkv_qkv_norm_rope_append): qkv bf16
+    [T][Hq + 2 Hkv][128] -> q_out bf16 [T][Hq][128]; K (normed, rotated) and
+    V are written into the pool."""
+    _need(qkv, torch.bfloat16, "qkv")
+    for t, n in ((cu_new, "cu_new"), (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _need(t, torch.int32, n)
+    for t, n in ((q_norm_w, "q_norm_w"), (k_norm_w, "k_norm_w"), (rope_cos, "rope_cos"),
+                 (rope_sin, "rope_sin")):
+        if t is not None:
+            _need(t, torch.float32, n)
+    T = qkv.shape[0]
+    if q_out is None:
+        q_out = torch.empty((T, num_q_heads, HEAD_DIM), dtype=torch.bfloat16, device=qkv.device)
+    pc = pool.c()
+    st = _lib.pkv_qkv_norm_rope_append(
+        ctypes.byref(pc), _ptr(qkv), T, num_q_heads, _ptr(q_norm_w), _ptr(k_norm_w), float(eps),
+        _ptr(rope_cos), _ptr(rope_sin), rope_cos.shape[0] if rope_cos is not None else 0,
+        _ptr(cu_new), seq_lens.shape[0], _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        _ptr(q_out), _stream(stream))
+    _check(st, "pkv_qkv_norm_rope_append")
+    return q_out
 
 
 def poll_device_error(stream=None) -> int:

@@ -284,3 +284,45 @@ def mixed_step(seed_index=5, prompt_len=26926, chunk=2048, R=32, Hq=32, Hkv=8,
             k_new=normal_bf16(rng, (n + R, Hkv, HEAD_DIM)),
             v_new=normal_bf16(rng, (n + R, Hkv, HEAD_DIM))))
     return wl
+
+
+# ------------------------------------------------ fused attention inputs
+
+def rope_tables(max_pos, base=1.0e6, D=HEAD_DIM):
+    """A model's RoPE cos/sin table, fp32 [max_pos][D/2]: angle p * base^(-2i/D)
+    (Qwen3-style base 1e6).  An input of the fused step, like its weights."""
+    inv = base ** (-np.arange(0, D, 2, dtype=np.float64) / D)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+@dataclass
+class QkvPrepCase:
+    Hq: int
+    Hkv: int
+    qkv: np.ndarray          # uint16 bf16 bits [T][Hq + 2 Hkv][D]
+    q_w: np.ndarray          # fp32 [D] (bf16-representable, like stored weights)
+    k_w: np.ndarray
+    cos: np.ndarray          # fp32 [max_pos][D/2]
+    sin: np.ndarray
+    cu_new: np.ndarray       # int32 [B+1]
+    seq_lens: np.ndarray     # int32 [B], new tokens included
+    layout: Layout
+
+
+def qkv_prep_case(seed, new_counts, totals, Hq=32, Hkv=8, max_pos=None):
+    """Seeded inputs of the fused attention-input step: a projection output
+    with N(0, 1) bf16 entries, norm weights U[0.5, 1.5] rounded to bf16, the
+    RoPE table, and scattered pages for sequences of `totals` positions whose
+    last `new_counts` are the new tokens."""
+    rng = np.random.default_rng(seed)
+    new_counts = np.asarray(new_counts, np.int32)
+    totals = np.asarray(totals, np.int32)
+    T = int(new_counts.sum())
+    qkv = normal_bf16(rng, (T, Hq + 2 * Hkv, HEAD_DIM))
+    q_w = bits_to_float(to_bf16_bits(rng.uniform(0.5, 1.5, HEAD_DIM).astype(np.float32)))
+    k_w = bits_to_float(to_bf16_bits(rng.uniform(0.5, 1.5, HEAD_DIM).astype(np.float32)))
+    cos, sin = rope_tables(int(totals.max()) if max_pos is None else max_pos)
+    layout = scatter_pages(rng, totals)
+    return QkvPrepCase(Hq, Hkv, qkv, q_w.astype(np.float32), k_w.astype(np.float32), cos, sin,
+                       cu_from_counts(new_counts), totals, layout)

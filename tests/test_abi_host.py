@@ -193,3 +193,30 @@ def test_status_strings(lib):
     f.restype = ctypes.c_char_p
     for s in (0, -1, -2, -3, -4):
         assert f(s)
+
+
+def test_qkv_prep_rejects_bad_arguments(lib):
+    f = lib.pkv_qkv_norm_rope_append
+    f.restype = ctypes.c_int32
+    V = ctypes.c_void_p
+    bf = good_pool()
+    #       qkv     T  Hq  q_w   k_w   eps                 cos     sin     maxpos cu
+    args = [V(FAKE), 4, 4, None, None, ctypes.c_float(1e-6), V(FAKE), V(FAKE), 64, V(FAKE),
+            1, V(FAKE), 4, V(FAKE), V(FAKE), None]
+    i8 = good_pool(dtype=1, k_scale=FAKE, v_scale=FAKE)
+    assert f(ctypes.byref(i8), *args) == UNSUPPORTED
+    bad = list(args)
+    bad[2] = 3                                        # Hq not a multiple of Hkv
+    assert f(ctypes.byref(bf), *bad) == INVALID
+    bad = list(args)
+    bad[7] = None                                     # cos without sin
+    assert f(ctypes.byref(bf), *bad) == INVALID
+    bad = list(args)
+    bad[5] = ctypes.c_float(-1.0)                     # negative eps
+    assert f(ctypes.byref(bf), *bad) == INVALID
+    bad = list(args)
+    bad[0] = V(FAKE + 2)                              # unaligned qkv
+    assert f(ctypes.byref(bf), *bad) == INVALID
+    none = list(args)
+    none[1] = 0                                       # no tokens: nothing to do
+    assert f(ctypes.byref(bf), *none) == 0

@@ -440,7 +440,7 @@ def _golden_rows():
             yield parts
 
 
-@pytest.mark.parametrize("row", list(range(3)))
+@pytest.mark.parametrize("row", list(range(4)))
 def test_norm_rope_golden_d4(row):
     x, w, c, s, want = list(_golden_rows())[row]
     D = 4
