@@ -4,7 +4,12 @@
 // table, split-KV for decode, and a combine kernel kept separate from the
 // split kernel; "INT8 KV cache": dequantisation inside attention).
 //
-// Split kernel: one CTA per (split, KV head, sequence), 4 warps.  A split is
+// Two split kernels: decode_split_kernel (bf16 pools, CUDA cores) and
+// decode_split_i8mma_kernel (INT8 pools, warp-level tensor-core MMAs; see
+// its own comment further down).  Both run one CTA per (split, KV head,
+// sequence), 4 warps, and share the warp merge and the combine.
+//
+// bf16 split kernel: one CTA per (split, KV head, sequence), 4 warps.  A split is
 // a run of consecutive logical pages of one sequence; the warps take its
 // pages round-robin and each warp streams its pages through a private ring
 // of shared-memory page buffers filled by the TMA engine (cp.async.bulk of
@@ -27,6 +32,9 @@
 #include <algorithm>
 #include <mutex>
 
+#include <cuda.h>
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -36,24 +44,20 @@ using namespace pkv;
 
 __device__ uint32_t g_err_decode;
 
-template <int G, bool INT8>
+template <int G>
 struct Cfg {
-  // lanes per key: INT8 with G = 4 uses 16 lanes (8 channels each), which
-  // halves the query/accumulator registers so more warps fit per SM
-  static constexpr int DL = (G <= 2) ? 4 : ((G == 4 && !INT8) ? 8 : 16);
+  static constexpr int DL = (G <= 2) ? 4 : (G == 4 ? 8 : 16);    // lanes per key
   static constexpr int KG = 32 / DL;                              // keys per pass
   static constexpr int PASSES = kPageSize / KG;
   static constexpr int DPL = kHeadDim / DL;                       // channels per lane
-  static constexpr int ESZ = INT8 ? 1 : 2;
-  static constexpr int LDB = (DPL * ESZ >= 16) ? 16 : DPL * ESZ;  // bytes per shared load
-  static constexpr int EPL = LDB / ESZ;                           // elements per load
+  static constexpr int LDB = 16;                                  // bytes per shared load
+  static constexpr int EPL = 8;                                   // bf16 elements per load
   static constexpr int NLD = DPL / EPL;                           // loads per lane per key
-  static constexpr int ROWB = kHeadDim * ESZ;                     // bytes per key row
+  static constexpr int ROWB = kHeadDim * 2;                       // bytes per key row
   static constexpr int SLAB = kPageSize * ROWB;                   // K or V slab bytes
-  static constexpr int SCB = INT8 ? kPageSize * 4 : 0;            // scale bytes per slab
-  static constexpr int BUF = 2 * SLAB + 2 * SCB;                  // one page of K, V (+scales)
+  static constexpr int BUF = 2 * SLAB;                            // one page of K and V
   static constexpr int HL = DL / G;                               // lanes per head after scatter
-  static constexpr int NBUF = INT8 ? (DL == 16 ? 3 : 5) : 3;      // page buffers per warp
+  static constexpr int NBUF = 3;                                  // page buffers per warp
   static_assert(NLD >= 1 && (NLD & (NLD - 1)) == 0, "loads per key must be a power of two");
   static_assert(BUF % 128 == 0, "page buffers stay 128-byte aligned");
 };
@@ -62,38 +66,13 @@ struct SplitArgs {
   pkv_host::DecodeLaunch a;
 };
 
-// Loads EPL consecutive elements at a shared address and widens them to fp32
-// pairs.  int8 codes are widened exactly (no scale applied here).
-template <bool INT8, int EPL>
-__device__ __forceinline__ void load_widen(const uint8_t* p, float2 (&x)[EPL / 2]) {
-  if constexpr (!INT8) {
-    static_assert(EPL == 8, "bf16 loads are 16 bytes");
-    const uint4 r = *reinterpret_cast<const uint4*>(p);
-    x[0] = make_float2(bf16lo(r.x), bf16hi(r.x));
-    x[1] = make_float2(bf16lo(r.y), bf16hi(r.y));
-    x[2] = make_float2(bf16lo(r.z), bf16hi(r.z));
-    x[3] = make_float2(bf16lo(r.w), bf16hi(r.w));
-  } else {
-    constexpr int NW = EPL / 4;
-    uint32_t w[NW];
-    if constexpr (EPL == 16) {
-      const uint4 r = *reinterpret_cast<const uint4*>(p);
-      w[0] = r.x; w[1] = r.y; w[2] = r.z; w[3] = r.w;
-    } else {
-      static_assert(EPL == 8, "int8 loads are 8 or 16 bytes");
-      const uint2 r = *reinterpret_cast<const uint2*>(p);
-      w[0] = r.x; w[1] = r.y;
-    }
-    const float2 bias = make_float2(-kI8Bias, -kI8Bias);
-#pragma unroll
-    for (int k = 0; k < NW; ++k) {
-      const uint32_t u = w[k] ^ 0x80808080u;
-      x[2 * k] = add2(make_float2(__uint_as_float(i8_biased_bits<0>(u)),
-                                  __uint_as_float(i8_biased_bits<1>(u))), bias);
-      x[2 * k + 1] = add2(make_float2(__uint_as_float(i8_biased_bits<2>(u)),
-                                      __uint_as_float(i8_biased_bits<3>(u))), bias);
-    }
-  }
+// Loads 8 consecutive bf16 at a shared address as four fp32 pairs.
+__device__ __forceinline__ void load_widen(const uint8_t* p, float2 (&x)[4]) {
+  const uint4 r = *reinterpret_cast<const uint4*>(p);
+  x[0] = make_float2(bf16lo(r.x), bf16hi(r.x));
+  x[1] = make_float2(bf16lo(r.y), bf16hi(r.y));
+  x[2] = make_float2(bf16lo(r.z), bf16hi(r.z));
+  x[3] = make_float2(bf16lo(r.w), bf16hi(r.w));
 }
 
 // Sum of v[g] over the DL lanes of a key, scattered: afterwards lane dl holds
@@ -121,9 +100,9 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[G], int dl) {
   return v[0];
 }
 
-template <int G, bool INT8>
+template <int G>
 struct WarpState {
-  using C = Cfg<G, INT8>;
+  using C = Cfg<G>;
   float2 q[C::NLD][C::EPL / 2][G];   // pre-scaled query, in this lane's chunk order
   float2 o[C::NLD][C::EPL / 2][G];   // unnormalised output accumulators
   float m = -INFINITY;               // running max (log2 domain) of head dl / HL
@@ -131,21 +110,19 @@ struct WarpState {
 };
 
 // One page of 16 keys (nvalid of them real) from shared memory.
-template <int G, bool INT8, bool PARTIAL>
-__device__ __forceinline__ void process_page(WarpState<G, INT8>& st, const uint8_t* buf,
+template <int G, bool PARTIAL>
+__device__ __forceinline__ void process_page(WarpState<G>& st, const uint8_t* buf,
                                              int nvalid, int kg, int dl) {
-  using C = Cfg<G, INT8>;
+  using C = Cfg<G>;
   const uint8_t* kbuf = buf;
   const uint8_t* vbuf = buf + C::SLAB;
-  const float* ksc = reinterpret_cast<const float*>(buf + 2 * C::SLAB);
-  const float* vsc = ksc + kPageSize;
   const int lane = kg * C::DL + dl;
 
   float s[C::PASSES];
 #pragma unroll
   for (int ps = 0; ps < C::PASSES; ++ps) {
     const int key = ps * C::KG + kg;
-    const uint8_t* row = kbuf + key * C::ROWB + dl * C::DPL * C::ESZ;
+    const uint8_t* row = kbuf + key * C::ROWB + dl * C::DPL * 2;
     float2 acc[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
@@ -153,7 +130,7 @@ __device__ __forceinline__ void process_page(WarpState<G, INT8>& st, const uint8
     for (int j = 0; j < C::NLD; ++j) {
       const int jj = (j + kg) & (C::NLD - 1);
       float2 x[C::EPL / 2];
-      load_widen<INT8, C::EPL>(row + jj * C::LDB, x);
+      load_widen(row + jj * C::LDB, x);
 #pragma unroll
       for (int i = 0; i < C::EPL / 2; ++i)
 #pragma unroll
@@ -162,8 +139,7 @@ __device__ __forceinline__ void process_page(WarpState<G, INT8>& st, const uint8
     float part[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) part[g] = acc[g].x + acc[g].y;
-    float sc = reduce_scatter<G, C::DL>(part, dl);
-    if constexpr (INT8) sc *= ksc[key];
+    const float sc = reduce_scatter<G, C::DL>(part, dl);
     s[ps] = (PARTIAL && key >= nvalid) ? -INFINITY : sc;
   }
 
@@ -204,17 +180,12 @@ __device__ __forceinline__ void process_page(WarpState<G, INT8>& st, const uint8
     for (int g = 0; g < G; ++g)
       pg[g] = __shfl_sync(0xffffffffu, p[ps], (lane & ~(C::DL - 1)) | (g * C::HL));
     if (!PARTIAL || key < nvalid) {
-      if constexpr (INT8) {
-        const float vs = vsc[key];
-#pragma unroll
-        for (int g = 0; g < G; ++g) pg[g] *= vs;
-      }
-      const uint8_t* row = vbuf + key * C::ROWB + dl * C::DPL * C::ESZ;
+      const uint8_t* row = vbuf + key * C::ROWB + dl * C::DPL * 2;
 #pragma unroll
       for (int j = 0; j < C::NLD; ++j) {
         const int jj = (j + kg) & (C::NLD - 1);
         float2 x[C::EPL / 2];
-        load_widen<INT8, C::EPL>(row + jj * C::LDB, x);
+        load_widen(row + jj * C::LDB, x);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float2 p2 = make_float2(pg[g], pg[g]);
@@ -226,13 +197,139 @@ __device__ __forceinline__ void process_page(WarpState<G, INT8>& st, const uint8
   }
 }
 
+// Log-sum-exp merge of n split partials of one (row, head) by a CTA of 128
+// threads (thread = channel): lp = their log2-domain lse [n], op = their
+// normalised O [n][128] (written by other CTAs: read through L2).  Block-wide
+// max, weights staged 128 splits at a time in shared memory (wsm, 128
+// floats; red, 4 floats), 8 partial rows in flight per thread.  Every thread
+// of the CTA must call it.  Returns (O, lse2) of channel threadIdx.x; lse2 =
+// -inf and O = 0 when no split holds a key.
+__device__ __forceinline__ float2 merge_splits(const float* lp, const float* op, int n,
+                                               float* wsm, float* red) {
+  static_assert(pkv_host::kDecodeWarps * 32 == 128, "one thread per channel");
+  const int d = threadIdx.x;
+  float M = -INFINITY;
+  for (int s = d; s < n; s += 128) M = fmaxf(M, __ldcg(lp + s));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  __syncthreads();                                   // red / wsm free (earlier use done)
+  if ((d & 31) == 0) red[d >> 5] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  if (M == -INFINITY) return make_float2(0.f, -INFINITY);   // uniform over the CTA
+  float sum = 0.f, O = 0.f;
+  for (int base = 0; base < n; base += 128) {
+    const int cnt = min(128, n - base);
+    __syncthreads();                                 // the previous chunk's weights are used
+    if (d < cnt) wsm[d] = fast_exp2(__ldcg(lp + base + d) - M);
+    __syncthreads();
+    const float* ob = op + (size_t)base * kHeadDim + d;
+    int j = 0;
+    for (; j + 8 <= cnt; j += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(ob + (size_t)(j + u) * kHeadDim);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        sum += wsm[j + u];
+        O += wsm[j + u] * v[u];
+      }
+    }
+    for (; j < cnt; ++j) {
+      sum += wsm[j];
+      O += wsm[j] * __ldcg(ob + (size_t)j * kHeadDim);
+    }
+  }
+  return make_float2(O / sum, M + fast_log2(sum));
+}
+
+// The CTA's merge of its warps: each warp has parked (O [G][128], m [G],
+// l [G]) at the start of its buffer area (bufs + w * warp_stride, log2
+// domain, O unnormalised); combine them, then write the bf16 output (one
+// split) or the split's partial, and with FUSED let the last split of the
+// (sequence, KV head) merge the partials.
+template <int G, bool FUSED>
+__device__ __forceinline__ void merge_warps(const pkv_host::DecodeLaunch& a, uint8_t* smem,
+                                            const uint8_t* bufs, size_t warp_stride, int split,
+                                            int h, int b, int nv, bool direct) {
+  constexpr int W = pkv_host::kDecodeWarps;
+  const int Hq = a.num_q_heads;
+  for (int t = threadIdx.x; t < G * kHeadDim; t += W * 32) {
+    const int g = t / kHeadDim, d = t % kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      const float* wmw = reinterpret_cast<const float*>(bufs + w * warp_stride) + G * kHeadDim;
+      M = fmaxf(M, wmw[g]);
+    }
+    float Lsum = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float* wow = reinterpret_cast<const float*>(bufs + w * warp_stride);
+        const float* wmw = wow + G * kHeadDim;
+        const float f = fast_exp2(wmw[g] - M);
+        Lsum += f * wmw[G + g];
+        O += f * wow[g * kHeadDim + d];
+      }
+      O = O / Lsum;
+    }
+    const float lse2 = (M == -INFINITY) ? -INFINITY : M + fast_log2(Lsum);
+    const int hq = h * G + g;
+    if (direct) {
+      static_cast<__nv_bfloat16*>(a.out)[((size_t)b * Hq + hq) * kHeadDim + d] =
+          __float2bfloat16_rn(O);
+      if (a.lse && d == 0) a.lse[(size_t)b * Hq + hq] = lse2 * kLn2;
+    } else {
+      const size_t row = ((size_t)b * Hq + hq) * a.splits + split;
+      a.ws_o[row * kHeadDim + d] = O;
+      if (d == 0) a.ws_lse[row] = lse2;
+    }
+  }
+  if (direct || !FUSED) return;                 // separate combine kernel
+
+  // Fused merge: count this split's part; the split that completes the count merges the
+  // nv parts of (b, KV head) (log-sum-exp rule, splits in order, so the
+  // result does not depend on which split merges) and resets the count.
+  // the flag sits in the unused end of the barrier header (no static shared
+  // memory: it would pad the 1024-byte aligned dynamic allocation)
+  volatile uint32_t& s_last = *reinterpret_cast<volatile uint32_t*>(smem + 1020);
+  static_assert(pkv_host::kDecodeWarps * 5 * 8 <= 1020, "barrier header");
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t* ctr = a.ws_ctr + (size_t)b * a.num_kv_heads + h;
+    uint32_t old;
+    asm volatile("fence.acq_rel.gpu;\n\tatom.relaxed.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(old) : "l"(ctr) : "memory");
+    const bool last = old == (uint32_t)(nv - 1);
+    if (last) {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      *ctr = 0u;                                  // ready for the next call
+    }
+    s_last = last ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // the warps' buffers are free now: weights and the block reduction use them
+  float* wsm = reinterpret_cast<float*>(const_cast<uint8_t*>(bufs));
+  float* red = wsm + 128;
+  for (int g = 0; g < G; ++g) {
+    const size_t bh = (size_t)b * Hq + h * G + g;
+    const float2 r = merge_splits(a.ws_lse + bh * a.splits, a.ws_o + bh * a.splits * kHeadDim,
+                                  nv, wsm, red);
+    const int d = threadIdx.x;
+    static_cast<__nv_bfloat16*>(a.out)[bh * kHeadDim + d] = __float2bfloat16_rn(r.x);
+    if (a.lse && d == 0) a.lse[bh] = r.y * kLn2;
+  }
+}
+
 // FUSED: the split that completes a (sequence, KV head) merges its splits
 // (a.ws_ctr counts them); otherwise a separate combine kernel does.  A
 // template parameter, so that the default kernel carries none of that code.
-template <int G, bool INT8, bool FUSED>
+template <int G, bool FUSED>
 __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
     decode_split_kernel(const __grid_constant__ pkv_host::DecodeLaunch a) {
-  using C = Cfg<G, INT8>;
+  using C = Cfg<G>;
   constexpr int W = pkv_host::kDecodeWarps;
   constexpr int NBUF = C::NBUF;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -300,10 +397,6 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
       mbar_arrive_expect_tx(bar, C::BUF);
       bulk_g2s_hint(dst, kpool + slab * C::SLAB, C::SLAB, bar, policy);
       bulk_g2s_hint(dst + C::SLAB, vpool + slab * C::SLAB, C::SLAB, bar, policy);
-      if constexpr (INT8) {
-        bulk_g2s(dst + 2 * C::SLAB, a.k_scale + slab * kPageSize, C::SCB, bar);
-        bulk_g2s(dst + 2 * C::SLAB + C::SCB, a.v_scale + slab * kPageSize, C::SCB, bar);
-      }
     }
   };
 
@@ -312,10 +405,9 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
   const int pro = min(NBUF, n_w);
   for (int i = 0; i < pro; ++i) issue(i, page_id(i));
   int issued = pro;
-  // Query rows of the group, pre-scaled by softmax_scale * log2(e) (and by
-  // the key smoothing weight, which the dequantised keys carry).  Loaded
+  // Query rows of the group, pre-scaled by softmax_scale * log2(e).  Loaded
   // after the first page copies are in flight, so their latency overlaps.
-  WarpState<G, INT8> st;
+  WarpState<G> st;
   {
     const float qs = a.softmax_scale * kLog2e;
     const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
@@ -325,22 +417,13 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
 #pragma unroll
       for (int j = 0; j < C::NLD; ++j) {
         const int jj = (j + kg) & (C::NLD - 1);
-        const int d0 = dl * C::DPL + jj * C::EPL;      // EPL is 8 or 16: whole 16-byte chunks
+        const int d0 = dl * C::DPL + jj * C::EPL;      // a whole 16-byte chunk
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + d0));
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-        for (int c8 = 0; c8 < C::EPL / 8; ++c8) {
-          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8 * c8));
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float x0 = bf16lo(w[e]) * qs, x1 = bf16hi(w[e]) * qs;
-            if (INT8 && a.k_smooth) {
-              const float2 ww = __ldg(reinterpret_cast<const float2*>(a.k_smooth + d0 + 8 * c8 + 2 * e));
-              x0 *= ww.x;
-              x1 *= ww.y;
-            }
-            st.q[j][4 * c8 + e][g] = make_float2(x0, x1);
-            st.o[j][4 * c8 + e][g] = make_float2(0.f, 0.f);
-          }
+        for (int e = 0; e < 4; ++e) {
+          st.q[j][e][g] = make_float2(bf16lo(w[e]) * qs, bf16hi(w[e]) * qs);
+          st.o[j][e][g] = make_float2(0.f, 0.f);
         }
       }
     }
@@ -359,9 +442,9 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
     const int nvalid = min(kPageSize, L - lp * kPageSize);
     const uint8_t* buf = wbuf + k * C::BUF;
     if (nvalid == kPageSize)
-      process_page<G, INT8, false>(st, buf, nvalid, kg, dl);
+      process_page<G, false>(st, buf, nvalid, kg, dl);
     else
-      process_page<G, INT8, true>(st, buf, nvalid, kg, dl);
+      process_page<G, true>(st, buf, nvalid, kg, dl);
     __syncwarp();
     if (issued < n_w) {
       issue(issued, page_id(issued));
@@ -442,83 +525,387 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
     }
   }
   __syncthreads();
+  merge_warps<G, FUSED>(a, smem, bufs, (size_t)NBUF * C::BUF, split, h, b, nv, direct);
+}
 
-  for (int t = threadIdx.x; t < G * kHeadDim; t += W * 32) {
-    const int g = t / kHeadDim, d = t % kHeadDim;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const float* wmw = reinterpret_cast<const float*>(bufs + (size_t)w * NBUF * C::BUF) +
-                         G * kHeadDim;
-      M = fmaxf(M, wmw[g]);
-    }
-    float Lsum = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float* wow = reinterpret_cast<const float*>(bufs + (size_t)w * NBUF * C::BUF);
-        const float* wmw = wow + G * kHeadDim;
-        const float f = fast_exp2(wmw[g] - M);
-        Lsum += f * wmw[G + g];
-        O += f * wow[g * kHeadDim + d];
-      }
-      O = O / Lsum;
-    }
-    const float lse2 = (M == -INFINITY) ? -INFINITY : M + fast_log2(Lsum);
-    const int hq = h * G + g;
-    if (direct) {
-      static_cast<__nv_bfloat16*>(a.out)[((size_t)b * Hq + hq) * kHeadDim + d] =
-          __float2bfloat16_rn(O);
-      if (a.lse && d == 0) a.lse[(size_t)b * Hq + hq] = lse2 * kLn2;
-    } else {
-      const size_t row = ((size_t)b * Hq + hq) * a.splits + split;
-      a.ws_o[row * kHeadDim + d] = O;
-      if (d == 0) a.ws_lse[row] = lse2;
-    }
-  }
-  if (direct || !FUSED) return;                 // separate combine kernel
+// ------------------------------------------------------------------------
+// INT8 split kernel on tensor cores (mma.sync m16n8k16, f16 in, f32 out).
+//
+// On CUDA cores the INT8 page loop is bound by instruction issue: widening
+// 4 KB of codes and the G-head dot products and reductions cost ~700 warp
+// instructions per page.  Here both products of a page run as warp MMAs:
+//   QK: A = the query rows (16 x 16 channels per k-step), B = the page's
+//       keys (16 channels x 8 keys), two key tiles x 8 k-steps = 16 MMAs;
+//   PV: A = V^T (16 channels x 16 keys), B = P' = p * v_scale (16 keys x
+//       8 heads), 8 channel tiles = 8 MMAs.
+// int8 codes become f16 exactly with a byte permute: 0x64XX is the f16
+// 1024 + XX, and XX = code ^ 0x80 = code + 128.  K subtracts the 1152 bias
+// in f16 (exact); V keeps it and the epilogue removes 1152 * sum(P'), using
+// the f16 P' values the MMAs saw.  The query is split into an f16 high part
+// and an f16 low part (q' = hi + lo to ~22 bits) placed in rows 0..G-1 and
+// G..2G-1 of A; the two rows' scores are added after the MMA, so the scores
+// keep fp32-like precision.  Rows 2G..15 are zero.
+//
+// Layouts follow the m16n8k16 fragments: lane = 4 r + qd.  In QK, B's k
+// index 2qd + e (+8) of k-step kb is channel 32 qd + 4 kb + e (+2), so a
+// lane converts whole 4-byte words of its 32-byte chunk of a key row; D
+// leaves lane (r, qd) with the scores of row r for keys 8t + 2qd + {0, 1},
+// which is exactly the B fragment PV needs (column r, those keys): P never
+// moves between lanes.  In PV, rows r and r + 8 of channel tile 2i + m are
+// channels 16 r + 4 i + 2 m and + 1.  K and V slabs arrive by TMA with
+// 128-byte swizzle (16-byte chunk c of row k at c ^ (k & 7)), which makes
+// every fragment load conflict-free.
+namespace i8mma {
 
-  // Fused merge: count this split's part; the split that completes the count merges the
-  // nv parts of (b, KV head) (log-sum-exp rule, splits in order, so the
-  // result does not depend on which split merges) and resets the count.
-  // the flag sits in the unused end of the barrier header (no static shared
-  // memory: it would pad the 1024-byte aligned dynamic allocation)
-  volatile uint32_t& s_last = *reinterpret_cast<volatile uint32_t*>(smem + 1020);
-  static_assert(pkv_host::kDecodeWarps * 5 * 8 <= 1020, "barrier header");
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t* ctr = a.ws_ctr + (size_t)b * a.num_kv_heads + h;
-    uint32_t old;
-    asm volatile("fence.acq_rel.gpu;\n\tatom.relaxed.gpu.global.add.u32 %0, [%1], 1;"
-                 : "=r"(old) : "l"(ctr) : "memory");
-    const bool last = old == (uint32_t)(nv - 1);
-    if (last) {
-      asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      *ctr = 0u;                                  // ready for the next call
-    }
-    s_last = last ? 1u : 0u;
+constexpr int NB = 3;                                   // page buffers per warp
+constexpr int SLAB = kPageSize * kHeadDim;              // 2 KiB: K or V of one (page, head)
+constexpr int KV = 2 * SLAB;                            // one page buffer (1 KiB aligned)
+constexpr int SC = 2 * kPageSize * 4;                   // K and V scales of one page
+constexpr int WARP_BYTES = NB * KV;
+constexpr int SMEM = 1024 + pkv_host::kDecodeWarps * NB * (KV + SC);
+constexpr uint32_t kMagic = 0x64646464u;                // f16 exponent byte of 1024
+constexpr uint32_t kBias2 = 0x64806480u;                // f16x2 (1152, 1152)
+constexpr float kBias = 1152.0f;
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two f16 pairs (exact codes) from a word of four int8 codes: bytes (0, 1)
+// and (2, 3).
+__device__ __forceinline__ void codes_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(__byte_perm(u, kMagic, 0x4140)), "r"(kBias2));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(__byte_perm(u, kMagic, 0x4342)), "r"(kBias2));
+}
+
+// Two keys' words of the same four channels -> four f16 pairs (key a low,
+// key b high) of 1152 + code, one per channel byte.
+__device__ __forceinline__ void codes_pair_f16(uint32_t wa, uint32_t wb, uint32_t (&c)[4]) {
+  const uint32_t tl = __byte_perm(wa, wb, 0x5140) ^ 0x80808080u;
+  const uint32_t th = __byte_perm(wa, wb, 0x7362) ^ 0x80808080u;
+  c[0] = __byte_perm(tl, kMagic, 0x4140);
+  c[1] = __byte_perm(tl, kMagic, 0x4342);
+  c[2] = __byte_perm(th, kMagic, 0x4140);
+  c[3] = __byte_perm(th, kMagic, 0x4342);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  const __half2 h = *reinterpret_cast<const __half2*>(&v);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+__device__ __forceinline__ void tma_slab(uint32_t dst, const CUtensorMap* map, int row,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+}  // namespace i8mma
+
+template <int G, bool FUSED>
+__global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32, 4)
+    decode_split_i8mma_kernel(const __grid_constant__ CUtensorMap tk,
+                              const __grid_constant__ CUtensorMap tv,
+                              const __grid_constant__ pkv_host::DecodeLaunch a) {
+  using namespace i8mma;
+  constexpr int W = pkv_host::kDecodeWarps;
+  constexpr uint32_t FULL = 0xffffffffu;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  uint8_t* bufs = smem + 1024;
+  float* scales = reinterpret_cast<float*>(bufs + W * WARP_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, qd = lane & 3;
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int Hq = a.num_q_heads;
+
+  int L = a.seq_lens[b];
+  if (L < 0 || L > a.max_pages * kPageSize) {
+    if (threadIdx.x == 0) atomicOr(&g_err_decode, kErrBadIndex);
+    L = 0;
   }
-  __syncthreads();
-  if (!s_last) return;
-  for (int t = threadIdx.x; t < G * kHeadDim; t += W * 32) {
-    const int g = t / kHeadDim, d = t % kHeadDim;
-    const size_t bh = (size_t)b * Hq + h * G + g;
-    const float* lp = a.ws_lse + bh * a.splits;
-    const float* op = a.ws_o + bh * a.splits * kHeadDim;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nv; ++sp) M = fmaxf(M, __ldcg(lp + sp));
-    float sum = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < nv; ++sp) {
-        const float f = fast_exp2(__ldcg(lp + sp) - M);
-        sum += f;
-        O += f * __ldcg(op + (size_t)sp * kHeadDim + d);
+  const int npages = (L + kPageSize - 1) / kPageSize;
+  const int p_begin = split * a.pages_per_split;
+  if (split > 0 && p_begin >= npages) return;   // empty split: the merge skips it
+  const int nv = max(1, (npages + a.pages_per_split - 1) / a.pages_per_split);
+  const bool direct = a.splits == 1 || nv == 1;
+  const int p_end = min(npages, p_begin + a.pages_per_split);
+  const int n_w = max(0, (p_end - p_begin - warp + W - 1) / W);   // pages of this warp
+
+  const uint32_t bar0 = smem_u32(bars + warp * NB);
+  uint8_t* wbuf = bufs + (size_t)warp * WARP_BYTES;
+  const uint32_t wbuf_s = smem_u32(wbuf);
+  const float* wsc = scales + warp * NB * (SC / 4);
+  const uint32_t wsc_s = smem_u32(wsc);
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < NB; ++k) mbar_init(bar0 + 8 * k, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
+  const uint64_t policy = l2_policy_evict_first();
+  int bt_cache = 0;
+  auto page_id = [&](int i) -> int {
+    if ((i & 31) == 0) {
+      const int lp = p_begin + warp + (i + lane) * W;
+      bt_cache = (i + lane < n_w) ? __ldg(bt_row + lp) : 0;
+    }
+    int pg = __shfl_sync(FULL, bt_cache, i & 31);
+    if (pg < 0 || pg >= a.num_pages) {
+      if (lane == 0) atomicOr(&g_err_decode, kErrBadIndex);
+      pg = 0;
+    }
+    return pg;
+  };
+  auto issue = [&](int i, int pg) {
+    if (lane == 0) {
+      const int k = i % NB;
+      const uint32_t bar = bar0 + 8 * k;
+      const int row = (pg * a.num_kv_heads + h) * kPageSize;
+      // the warp's generic-proxy reads of this buffer are done (__syncwarp);
+      // order them before the async-proxy refill
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(bar, KV + SC);
+      tma_slab(wbuf_s + k * KV, &tk, row, bar, policy);
+      tma_slab(wbuf_s + k * KV + SLAB, &tv, row, bar, policy);
+      bulk_g2s(wsc_s + k * SC, a.k_scale + row, SC / 2, bar);
+      bulk_g2s(wsc_s + k * SC + SC / 2, a.v_scale + row, SC / 2, bar);
+    }
+  };
+  const int pro = min(NB, n_w);
+  for (int i = 0; i < pro; ++i) issue(i, page_id(i));
+  int issued = pro;
+
+  // A fragments of the query: row rr < G is head rr's high part, G <= rr <
+  // 2G head rr - G's low part; per k-step kb, lane (r, qd) holds channels
+  // 32 qd + 4 kb + {0, 1} (a0a1 / a2a3) and + {2, 3} (a4a5 / a6a7) of rows
+  // r and r + 8.  Pre-scaled by softmax_scale * log2(e) and the key
+  // smoothing weight.
+  uint32_t qa[8][4];
+  {
+    const float qs = a.softmax_scale * kLog2e;
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int rr = r + 8 * half;
+      int g = -1;
+      bool low = false;
+      if (half == 0 || G == 8) {
+        if (rr < G) {
+          g = rr;
+        } else if (rr < 2 * G) {
+          g = rr - G;
+          low = true;
+        }
       }
-      O = O / sum;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        uint32_t v01 = 0, v23 = 0;
+        if (g >= 0) {
+          const int c0 = 32 * qd + 4 * kb;
+          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(
+              qb + ((size_t)b * Hq + h * G + g) * kHeadDim + c0));
+          float x[4] = {bf16lo(raw.x) * qs, bf16hi(raw.x) * qs, bf16lo(raw.y) * qs,
+                        bf16hi(raw.y) * qs};
+          if (a.k_smooth) {
+            const float2 w01 = __ldg(reinterpret_cast<const float2*>(a.k_smooth + c0));
+            const float2 w23 = __ldg(reinterpret_cast<const float2*>(a.k_smooth + c0 + 2));
+            x[0] *= w01.x;
+            x[1] *= w01.y;
+            x[2] *= w23.x;
+            x[3] *= w23.y;
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float hi = __half2float(__float2half_rn(x[e]));
+            x[e] = low ? x[e] - hi : hi;
+          }
+          v01 = pack_f16x2(x[0], x[1]);
+          v23 = pack_f16x2(x[2], x[3]);
+        }
+        qa[kb][half] = v01;
+        qa[kb][2 + half] = v23;
+      }
     }
-    static_cast<__nv_bfloat16*>(a.out)[bh * kHeadDim + d] = __float2bfloat16_rn(O);
-    if (a.lse && d == 0) a.lse[bh] = (M == -INFINITY) ? -INFINITY : (M + fast_log2(sum)) * kLn2;
   }
+
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[mt][j] = 0.f;
+  float m_used = -INFINITY, l = 0.f, cs = 0.f;
+
+  bool failed = false;
+  int i_fail = 0;
+  for (int i = 0; i < n_w; ++i) {
+    const int k = i % NB;
+    if (!mbar_wait(bar0 + 8 * k, (uint32_t)(i / NB) & 1u)) {
+      failed = true;
+      i_fail = i;
+      break;
+    }
+    const int lp = p_begin + warp + i * W;
+    const int nvalid = min(kPageSize, L - lp * kPageSize);
+    const uint8_t* kbuf = wbuf + k * KV;
+    const uint8_t* vbuf = kbuf + SLAB;
+    const float* sc = wsc + k * (SC / 4);
+
+    // QK: two tiles of 8 keys; key 8t + r's row, chunks 2qd and 2qd + 1
+    float d[2][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d[t][j] = 0.f;
+      const uint8_t* row = kbuf + (8 * t + r) * kHeadDim;
+      const uint4 x0 = lds128(row + (((2 * qd) ^ r) << 4));
+      const uint4 x1 = lds128(row + (((2 * qd + 1) ^ r) << 4));
+      const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb) {
+        uint32_t blo, bhi;
+        codes_f16(w[kb], blo, bhi);
+        mma16816(d[t], qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], blo, bhi);
+      }
+    }
+    // scores of head row r for keys 8t + 2qd + e: high + low rows, times the
+    // key scale; keys past the sequence are masked
+    const float2 ksc[2] = {*reinterpret_cast<const float2*>(sc + 2 * qd),
+                           *reinterpret_cast<const float2*>(sc + 8 + 2 * qd)};
+    const float2 vsc[2] = {*reinterpret_cast<const float2*>(sc + 16 + 2 * qd),
+                           *reinterpret_cast<const float2*>(sc + 24 + 2 * qd)};
+    float s[2][2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = d[t][e];
+        if constexpr (G == 8)
+          v += d[t][e + 2];
+        else
+          v += __shfl_xor_sync(FULL, d[t][e], 4 * G);
+        v *= e ? ksc[t].y : ksc[t].x;
+        s[t][e] = (8 * t + 2 * qd + e < nvalid) ? v : -INFINITY;
+      }
+    float pm = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+    pm = fmaxf(pm, __shfl_xor_sync(FULL, pm, 1));
+    pm = fmaxf(pm, __shfl_xor_sync(FULL, pm, 2));
+    // the max the exponentials are taken against moves only when the page
+    // max passes it by more than 2^8 (p <= 256; exact: l and O share it)
+    const bool grow = pm > m_used + 8.f;
+    float alpha = 1.f;
+    if (grow) {
+      alpha = fast_exp2(m_used - pm);
+      m_used = pm;
+      l *= alpha;
+      cs *= alpha;
+    }
+    if (__any_sync(FULL, grow)) {
+      const float a0 = __shfl_sync(FULL, alpha, 8 * qd);       // head 2qd's row
+      const float a1 = __shfl_sync(FULL, alpha, 8 * qd + 4);   // head 2qd + 1's row
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+    }
+    float pv[2][2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float p = fast_exp2(s[t][e] - m_used);
+        l += p;
+        // masked keys: p = 0, and their (unwritten) scale must not reach the MMA
+        pv[t][e] = (8 * t + 2 * qd + e < nvalid) ? p * (e ? vsc[t].y : vsc[t].x) : 0.f;
+      }
+    const uint32_t pb0 = pack_f16x2(pv[0][0], pv[0][1]);
+    const uint32_t pb1 = pack_f16x2(pv[1][0], pv[1][1]);
+    {
+      const float2 f0 = unpack_f16x2(pb0), f1 = unpack_f16x2(pb1);
+      cs += (f0.x + f0.y) + (f1.x + f1.y);
+    }
+
+    // PV: chunk r of keys 2qd, 2qd + 1, 2qd + 8, 2qd + 9
+    const int k0 = 2 * qd;
+    const uint4 va = lds128(vbuf + k0 * kHeadDim + ((r ^ k0) << 4));
+    const uint4 vb = lds128(vbuf + (k0 + 1) * kHeadDim + ((r ^ (k0 + 1)) << 4));
+    const uint4 vc = lds128(vbuf + (k0 + 8) * kHeadDim + ((r ^ k0) << 4));
+    const uint4 vd = lds128(vbuf + (k0 + 9) * kHeadDim + ((r ^ (k0 + 1)) << 4));
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+    const uint32_t wc[4] = {vc.x, vc.y, vc.z, vc.w}, wd[4] = {vd.x, vd.y, vd.z, vd.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t c[4], e[4];
+      codes_pair_f16(wa[j], wb[j], c);
+      codes_pair_f16(wc[j], wd[j], e);
+      mma16816(o[2 * j], c[0], c[1], e[0], e[1], pb0, pb1);
+      mma16816(o[2 * j + 1], c[2], c[3], e[2], e[3], pb0, pb1);
+    }
+    __syncwarp();
+    if (issued < n_w) {
+      issue(issued, page_id(issued));
+      ++issued;
+    }
+  }
+  if (failed) {
+    if (lane == 0) atomicOr(&g_err_decode, kErrTimeout);
+    for (int i = i_fail; i < issued; ++i)
+      (void)mbar_wait(bar0 + 8 * (i % NB), (uint32_t)(i / NB) & 1u);
+  }
+  __syncwarp();
+
+  // Park (O - 1152 sum P', m, l) of the warp's G heads in its buffers (all of
+  // its copies have landed), then merge the warps.
+  l += __shfl_xor_sync(FULL, l, 1);
+  l += __shfl_xor_sync(FULL, l, 2);
+  cs += __shfl_xor_sync(FULL, cs, 1);
+  cs += __shfl_xor_sync(FULL, cs, 2);
+  const float bA = kBias * __shfl_sync(FULL, cs, 8 * qd);
+  const float bB = kBias * __shfl_sync(FULL, cs, 8 * qd + 4);
+  float* wo = reinterpret_cast<float*>(wbuf);              // [G][128]
+  float* wm = wo + G * kHeadDim;                           // [G]
+  float* wl = wm + G;                                      // [G]
+  const int c0 = 2 * qd, c1 = 2 * qd + 1;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int ch = 16 * r + 4 * (mt >> 1) + 2 * (mt & 1);
+    if (c0 < G)
+      *reinterpret_cast<float2*>(wo + c0 * kHeadDim + ch) =
+          failed ? make_float2(0.f, 0.f) : make_float2(o[mt][0] - bA, o[mt][2] - bA);
+    if (c1 < G)
+      *reinterpret_cast<float2*>(wo + c1 * kHeadDim + ch) =
+          failed ? make_float2(0.f, 0.f) : make_float2(o[mt][1] - bB, o[mt][3] - bB);
+  }
+  if (qd == 0 && r < G) {
+    wm[r] = failed ? -INFINITY : m_used;
+    wl[r] = failed ? 0.f : l;
+  }
+  __syncthreads();
+  merge_warps<G, FUSED>(a, smem, bufs, (size_t)WARP_BYTES, split, h, b, nv, direct);
 }
 
 // Combine (separate kernel): out = sum_s 2^(lse_s - lse) * O_s, lse = log2
@@ -526,6 +913,7 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
 // of them); rows whose keys fit one split were finished by that split.
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__
                                                              pkv_host::DecodeLaunch a) {
+  __shared__ float wsm[128], red[4];
   const int bh = blockIdx.x;
   const int b = bh / a.num_q_heads;
   const int d = threadIdx.x;
@@ -534,52 +922,75 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
   const int npages = (L + kPageSize - 1) / kPageSize;
   const int n = min(a.splits, (npages + a.pages_per_split - 1) / a.pages_per_split);
   if (n <= 1) return;                           // one split: it wrote the output itself
-  const float* lp = a.ws_lse + (size_t)bh * a.splits;
-  const float* op = a.ws_o + (size_t)bh * a.splits * kHeadDim;
-  float M = -INFINITY;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, lp[s]);
-  float sum = 0.f, O = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n; ++s) {
-      const float f = fast_exp2(lp[s] - M);
-      sum += f;
-      O += f * op[(size_t)s * kHeadDim + d];
-    }
-    O = O / sum;
-  }
-  static_cast<__nv_bfloat16*>(a.out)[(size_t)bh * kHeadDim + d] = __float2bfloat16_rn(O);
-  if (a.lse && d == 0)
-    a.lse[bh] = (M == -INFINITY) ? -INFINITY : (M + fast_log2(sum)) * kLn2;
+  const float2 r = merge_splits(a.ws_lse + (size_t)bh * a.splits,
+                                a.ws_o + (size_t)bh * a.splits * kHeadDim, n, wsm, red);
+  static_cast<__nv_bfloat16*>(a.out)[(size_t)bh * kHeadDim + d] = __float2bfloat16_rn(r.x);
+  if (a.lse && d == 0) a.lse[bh] = r.y * kLn2;
 }
 
-template <int G, bool INT8, bool FUSED>
+template <int G, bool FUSED>
 cudaError_t launch_split_as(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
-  using C = Cfg<G, INT8>;
+  using C = Cfg<G>;
   constexpr int smem = 1024 + pkv_host::kDecodeWarps * C::NBUF * C::BUF;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, INT8, FUSED>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, FUSED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
   dim3 grid(a.splits, a.num_kv_heads, a.batch);
-  decode_split_kernel<G, INT8, FUSED><<<grid, pkv_host::kDecodeWarps * 32, smem, s>>>(a);
+  decode_split_kernel<G, FUSED><<<grid, pkv_host::kDecodeWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
-template <int G, bool INT8>
+template <int G>
 cudaError_t launch_split(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
-  return a.ws_ctr ? launch_split_as<G, INT8, true>(a, s) : launch_split_as<G, INT8, false>(a, s);
+  return a.ws_ctr ? launch_split_as<G, true>(a, s) : launch_split_as<G, false>(a, s);
 }
 
-template <bool INT8>
+template <int G, bool FUSED>
+cudaError_t launch_i8mma_as(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_i8mma_kernel<G, FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, i8mma::SMEM);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  if ((long long)a.num_pages * a.num_kv_heads * kPageSize >= (1ll << 31))
+    return cudaErrorNotSupported;
+  CUtensorMap tk, tv;
+  if (!pkv_host::encode_int8_slab_map(&tk, a.k, a.num_pages, a.num_kv_heads) ||
+      !pkv_host::encode_int8_slab_map(&tv, a.v, a.num_pages, a.num_kv_heads))
+    return cudaErrorInvalidValue;
+  dim3 grid(a.splits, a.num_kv_heads, a.batch);
+  decode_split_i8mma_kernel<G, FUSED>
+      <<<grid, pkv_host::kDecodeWarps * 32, i8mma::SMEM, s>>>(tk, tv, a);
+  return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_i8mma(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
+  return a.ws_ctr ? launch_i8mma_as<G, true>(a, s) : launch_i8mma_as<G, false>(a, s);
+}
+
+cudaError_t dispatch_i8mma(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
+  switch (a.num_q_heads / a.num_kv_heads) {
+    case 1: return launch_i8mma<1>(a, s);
+    case 2: return launch_i8mma<2>(a, s);
+    case 4: return launch_i8mma<4>(a, s);
+    case 8: return launch_i8mma<8>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t dispatch_group(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_split<1, INT8>(a, s);
-    case 2: return launch_split<2, INT8>(a, s);
-    case 4: return launch_split<4, INT8>(a, s);
-    case 8: return launch_split<8, INT8>(a, s);
+    case 1: return launch_split<1>(a, s);
+    case 2: return launch_split<2>(a, s);
+    case 4: return launch_split<4>(a, s);
+    case 8: return launch_split<8>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -592,7 +1003,7 @@ bool decode_supports_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8;
 
 cudaError_t launch_decode(const DecodeLaunch& a, bool int8, cudaStream_t s) {
   if (a.batch == 0) return cudaSuccess;
-  cudaError_t e = int8 ? dispatch_group<true>(a, s) : dispatch_group<false>(a, s);
+  cudaError_t e = int8 ? dispatch_i8mma(a, s) : dispatch_group(a, s);
   if (e != cudaSuccess || a.splits == 1 || a.ws_ctr) return e;
   decode_combine_kernel<<<a.batch * a.num_q_heads, 128, 0, s>>>(a);
   return cudaGetLastError();

@@ -54,6 +54,12 @@ struct DecodeLaunch {
 constexpr int kDecodeWarps = 4;          // warps per split CTA
 constexpr int kDecodeCtasPerSm = 2;      // resident split CTAs per SM (by smem)
 
+// cuTensorMapEncodeTiled of an INT8 pool (K or V) as 2-D uint8 rows of 128
+// bytes, one box per (page, head) slab of 16 rows, 128B-swizzled; `map`
+// points to a CUtensorMap.  False if the driver entry point is missing or
+// rejects the arguments.
+bool encode_int8_slab_map(void* map, const void* base, int num_pages, int hkv);
+
 bool decode_supports_group(int group);
 cudaError_t launch_decode(const DecodeLaunch& a, bool int8, cudaStream_t s);
 uint32_t take_decode_error(cudaStream_t s);

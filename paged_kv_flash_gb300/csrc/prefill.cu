@@ -1185,6 +1185,30 @@ bool encode_q_map(CUtensorMap* m, const void* q, int total_q, int hq) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+namespace pkv_host {
+
+// An INT8 pool as a 2-D uint8 tensor of (num_pages * Hkv * 16) rows of 128
+// bytes; a box is one (page, head) slab of 16 rows, 128B-swizzled (the INT8
+// decode kernel reads it).
+bool encode_int8_slab_map(void* map, const void* base, int num_pages, int hkv) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_pages * hkv * kPageSize};
+  cuuint64_t strides[1] = {(cuuint64_t)kHeadDim};
+  cuuint32_t box[2] = {(cuuint32_t)kHeadDim, (cuuint32_t)kPageSize};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace pkv_host
+
+namespace {
+
 // Workspace: per-(CTA, tile) part counters, then the parts' lse, then their O.
 size_t ws_counter_bytes(int ctas) { return ((size_t)2 * ctas * 4 + 255) / 256 * 256; }
 size_t ws_lse_bytes(int ctas) { return (size_t)ctas * SLOT_ROWS * 4; }

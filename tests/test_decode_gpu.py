@@ -18,7 +18,7 @@ def pk():
     return pagedkv
 
 
-def gpu_decode(pk, case: W.DecodeCase, num_splits=0, int8_pools=None, smooth=None):
+def gpu_decode(pk, case: W.DecodeCase, num_splits=0, int8_pools=None, smooth=None, fused=False):
     if int8_pools is None:
         pool = pk.Pool(dev_bf16(case.k_pool), dev_bf16(case.v_pool))
     else:
@@ -26,7 +26,7 @@ def gpu_decode(pk, case: W.DecodeCase, num_splits=0, int8_pools=None, smooth=Non
     out, lse = pk.paged_attn_decode(pool, dev_bf16(case.q), dev(case.layout.block_table),
                                     dev(case.seq_lens), int(case.seq_lens.max()), case.scale,
                                     k_smooth=dev(smooth) if smooth is not None else None,
-                                    num_splits=num_splits)
+                                    num_splits=num_splits, fused=fused)
     assert pk.poll_device_error() == pk.OK
     return out, lse
 
@@ -149,7 +149,7 @@ def test_int8_32k_batch8_sampled(pk):
     check_lse(lse[idx], rl, "int8 32k b8")
 
 
-@pytest.mark.parametrize("G", [1, 2, 8])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_int8_group_sizes_ragged(pk, G):
     rng = np.random.default_rng(50 + G)
     lens = np.array([1, 17, 200, 513], np.int32)
@@ -164,10 +164,10 @@ def test_int8_group_sizes_ragged(pk, G):
     q = W.normal_bf16(rng, (4, 2 * G, W.HEAD_DIM))
     case = W.DecodeCase(2 * G, 2, lens, layout, q, None, None)
     ro, rl = oracle_decode(case, int8_pools=pools, smooth=w)
-    for splits in (0, 3):
-        out, lse = gpu_decode(pk, case, splits, int8_pools=pools, smooth=w)
-        check_out(out, ro, f"int8 G={G}")
-        check_lse(lse, rl, f"int8 G={G}")
+    for splits, fused in ((0, False), (3, False), (3, True), (1, False)):
+        out, lse = gpu_decode(pk, case, splits, int8_pools=pools, smooth=w, fused=fused)
+        check_out(out, ro, f"int8 G={G} splits={splits} fused={fused}")
+        check_lse(lse, rl, f"int8 G={G} splits={splits} fused={fused}")
 
 
 def test_fused_decode_workspace_reuse_is_exact():
