@@ -18,8 +18,9 @@ The JSON line reports the step time (value, us per step) and, from CUDA
 events around every call, decode HBM GB/s and prefill TFLOP/s; the roofline
 object is for the prefill kernel, which dominates the step.  "configs" holds
 the other workloads (single-sequence decode, 1,024-token prefill, batched
-decode, INT8 32k decode, the fused attention-input step on a 2,048-token
-chunk) timed with a 512 MB L2 flush between runs.
+decode, INT8 32k decode, 16-token verify steps through the multi-token
+decode, the fused attention-input step on a 2,048-token chunk) timed with a
+512 MB L2 flush between runs.
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 """
 import argparse
@@ -429,6 +430,12 @@ def other_configs(torch, pk, hbm, bf16):
         "append_us": round(a_med, 2), "append_GBps": round(2 * 2 * 1024 * 8 * 256 / a_med / 1e3, 1)}
     assert pk.poll_device_error() == pk.OK
     del pool
+    # verify steps (multi-token decode), with the prefill kernel on the same step
+    rng = np.random.default_rng(1006)
+    for name, lens, qlens in (("verify_16tok_1k_b1_gqa32x8", [1024], [16]),
+                              ("verify_16tok_b8_ctx4k_8k_gqa32x8",
+                               rng.integers(4096, 8193, 8), [16] * 8)):
+        res[name] = verify_entry(torch, pk, rng, lens, qlens, flush, hbm, bf16)
     # fused attention inputs for one 2,048-token chunk at positions 14,336..16,383
     fn, byts = qkv_prep_fn(torch, pk, 95)
     med, mn = time_events(torch, fn, flush=flush)
@@ -439,6 +446,36 @@ def other_configs(torch, pk, hbm, bf16):
                  "GQA 32/8; bytes = projection read + q_out, K, V writes + RoPE rows")}
     assert pk.poll_device_error() == pk.OK
     return res
+
+
+def verify_entry(torch, pk, rng, lens, qlens, flush, hbm, bf16, Hq=32, Hkv=8):
+    """A step of qlens[b] tokens per sequence through the multi-token decode
+    (split kernel + combine), and the same step through the prefill kernel."""
+    case = W.multi_token_decode(rng, lens, qlens, Hq, Hkv)
+    pool = pk.Pool(to_dev_bf16(torch, case.k_pool), to_dev_bf16(torch, case.v_pool))
+    q, cu = to_dev_bf16(torch, case.q), to_dev(torch, case.cu_q)
+    bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
+    mq, ms = int(max(qlens)), int(max(lens))
+    S, C, wsb = pk.decode_multi_plan(len(lens), len(case.q), Hq, Hkv, mq, ms)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((len(case.q), Hq), dtype=torch.float32, device="cuda")
+    fm = lambda: pk.paged_attn_decode_multi(pool, q, cu, bt, sl, mq, ms, SCALE, workspace=ws,
+                                            out=out, lse=lse)
+    wsp = pk.prefill_workspace()
+    fp = lambda: pk.paged_attn_prefill(pool, q, cu, bt, sl, mq, SCALE, workspace=wsp, out=out,
+                                       lse=lse)
+    m_med, m_min = time_events(torch, fm, flush=flush)
+    p_med, _ = time_events(torch, fp, flush=flush)
+    assert pk.poll_device_error() == pk.OK
+    byts = decode_bytes(lens, Hkv)
+    fl = sum(prefill_flops(qn, L, Hq) for qn, L in zip(qlens, lens))
+    return {"us": round(m_med, 2), "us_min": round(m_min, 2), "GBps": round(byts / m_med / 1e3, 1),
+            "frac_of_measured": round(byts / m_med / 1e3 / hbm, 4), "bytes": int(byts),
+            "TFLOPs": round(fl / m_med / 1e6, 1), "splits": S,
+            "prefill_kernel_us": round(p_med, 2),
+            "note": ("multi-token decode (pkv_paged_attn_decode_multi): split kernel + combine; "
+                     "prefill_kernel_us = the same step through pkv_paged_attn_prefill")}
 
 
 def qkv_prep_fn(torch, pk, seed, T=2048, L=16384, Hq=32, Hkv=8):

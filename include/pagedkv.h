@@ -256,6 +256,51 @@ pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, int32_t t
                                   void* out, float* lse, void* stream);
 
 /*
+ * decode_multi_plan -- split plan and workspace size of a multi-token decode
+ * (pkv_paged_attn_decode_multi): batch sequences holding total_q query
+ * tokens in all, at most max_q_len (1..16) each.  num_splits 0 = heuristic
+ * (the single-token plan with ceil(max_q_len * G / 64) CTAs per sequence
+ * and KV head), > 0 forces.  workspace_bytes_out: 0 when one split is used.
+ * PKV_ERR_UNSUPPORTED for max_q_len > 16.  Host only.
+ */
+pkv_status pkv_decode_multi_plan(int32_t batch, int32_t total_q, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t max_q_len, int32_t max_seq_len,
+                                 int32_t num_splits, int32_t* splits_out,
+                                 int32_t* pages_per_split_out, size_t* workspace_bytes_out);
+
+/*
+ * paged_attn_decode_multi -- attention for steps of 1..16 query tokens per
+ * sequence through split-KV decode ("Attention for verify steps": steps of
+ * 2-16 tokens, verify steps of speculative decoding among them, run the
+ * split-KV decode kernels rather than the prefill kernel), plus the
+ * log-sum-exp combine.  Causal inside the step, bottom-right aligned: token
+ * i of the q_b tokens of sequence b (seq_lens[b] positions, these tokens
+ * included, appended beforehand) sees positions 0 .. seq_lens[b] - q_b + i.
+ *
+ *  q          bf16 [total_q][num_q_heads][128], 16-byte aligned; sequence b
+ *             owns rows cu_q[b] .. cu_q[b+1] - 1 (cu_q int32 [batch + 1],
+ *             non-decreasing, cu_q[0] = 0).
+ *  block_table, max_pages, seq_lens, max_seq_len, softmax_scale: as
+ *             pkv_paged_attn_decode.  max_q_len: the largest q_b (1..16).
+ *  num_splits, workspace: as pkv_decode_multi_plan (256-byte aligned
+ *             workspace of its size when splits > 1, else may be NULL).
+ *  out        bf16 [total_q][num_q_heads][128]; lse fp32 [total_q][Hq]
+ *             (natural log) or NULL.
+ * bf16 pools only (PKV_ERR_UNSUPPORTED for INT8 and for max_q_len > 16).
+ * A sequence with q_b > max_q_len, seq_lens[b] < q_b, a length past the
+ * block table or a page id outside the pool is skipped and flagged for
+ * pkv_poll_device_error.
+ */
+pkv_status pkv_paged_attn_decode_multi(const pkv_pool* pool, const void* q, int32_t total_q,
+                                       const int32_t* cu_q, int32_t batch, int32_t num_q_heads,
+                                       const int32_t* block_table, int32_t max_pages,
+                                       const int32_t* seq_lens, int32_t max_q_len,
+                                       int32_t max_seq_len, float softmax_scale,
+                                       int32_t num_splits, void* workspace,
+                                       size_t workspace_bytes, void* out, float* lse,
+                                       void* stream);
+
+/*
  * qkv_norm_rope_append -- the fused attention-input step: from the fused
  * q/k/v projection output, per-head RMSNorm of q and k, RoPE, and the KV
  * cache write, in one kernel ("Fused kernels ...": the attention-input

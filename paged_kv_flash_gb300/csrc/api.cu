@@ -116,6 +116,60 @@ void set_workspace(pkv_host::DecodeLaunch& a, const Plan& p, void* ws, bool fuse
   a.ws_lse = p.ws_bytes ? reinterpret_cast<float*>(base + p.ws_lse_offset) : nullptr;
 }
 
+// Plan of a multi-token decode.  Its kernel fits three CTAs per SM; a CTA
+// of T row tiles (16 rows each, T <= 4) puts Tp = 1, 2 or 4 warps on every
+// page, so a page costs it more as the step grows.  Pages per split: the
+// single-token rule (about 0.8 CTAs per resident slot, 8..128 pages) on
+// three slots per SM, divided by Tp / 2 (at least 4 pages), a multiple of
+// 4.  A GB300 sweep of forced split counts put the optimum there for steps
+// of 1, 8 and 16 tokens.  Workspace: total_q x Hq rows of split partials.
+constexpr int kMultiMaxQ = 16;
+constexpr int kMultiRowsPerCta = 64;
+constexpr int kMultiCtasPerSm = 3;
+
+struct MultiPlan {
+  Plan p;
+  int row_groups;
+};
+
+MultiPlan make_multi_plan(int batch, int total_q, int num_q_heads, int num_kv_heads, int max_q,
+                          int max_seq_len, int num_splits) {
+  MultiPlan m;
+  const int G = num_q_heads / num_kv_heads;
+  const int rows = max_q * G;
+  m.row_groups = std::max(1, (rows + kMultiRowsPerCta - 1) / kMultiRowsPerCta);
+  const int T = (std::min(rows, kMultiRowsPerCta) + 15) / 16;
+  const int Tp = T <= 1 ? 1 : (T == 2 ? 2 : 4);
+  const int mp = std::max(1, (max_seq_len + pkv::kPageSize - 1) / pkv::kPageSize);
+  int C;
+  if (num_splits > 0) {
+    C = (mp + num_splits - 1) / num_splits;
+  } else {
+    const long long slots = (long long)sm_count() * kMultiCtasPerSm;
+    const long long target = std::max<long long>(1, slots * kPlanSlotsNum / kPlanSlotsDen);
+    const long long units = (long long)batch * m.row_groups * num_kv_heads;
+    long long c = (units * mp + target - 1) / target;
+    c = std::max<long long>(kPlanMinPages, std::min<long long>(kPlanMaxPages, c));
+    c = std::max<long long>(4, c / std::max(1, Tp / 2));
+    c = (c + 3) / 4 * 4;
+    C = (int)std::min<long long>(c, mp);
+  }
+  C = std::max(1, C);
+  Plan& p = m.p;
+  p.splits = (mp + C - 1) / C;
+  p.pages_per_split = C;
+  p.ws_zero_bytes = 0;
+  if (p.splits == 1) {
+    p.ws_bytes = p.ws_o_offset = p.ws_lse_offset = 0;
+  } else {
+    const size_t n = (size_t)total_q * num_q_heads * p.splits;
+    p.ws_o_offset = 0;
+    p.ws_lse_offset = (n * pkv::kHeadDim * sizeof(float) + 255) / 256 * 256;
+    p.ws_bytes = p.ws_lse_offset + (n * sizeof(float) + 255) / 256 * 256;
+  }
+  return m;
+}
+
 }  // namespace
 
 extern "C" {
@@ -353,11 +407,81 @@ pkv_status pkv_qkv_norm_rope_append(const pkv_pool* pool, const void* qkv, int32
   return cuda_status(pkv_host::launch_qkv_prep(a, static_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_decode_multi_plan(int32_t batch, int32_t total_q, int32_t num_q_heads,
+                                 int32_t num_kv_heads, int32_t max_q_len, int32_t max_seq_len,
+                                 int32_t num_splits, int32_t* splits_out,
+                                 int32_t* pages_per_split_out, size_t* workspace_bytes_out) {
+  if (batch < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads || max_q_len < 1 || max_seq_len < 0 || num_splits < 0)
+    return PKV_ERR_INVALID;
+  if (max_q_len > kMultiMaxQ) return PKV_ERR_UNSUPPORTED;
+  const MultiPlan m = make_multi_plan(batch, total_q, num_q_heads, num_kv_heads, max_q_len,
+                                      max_seq_len, num_splits);
+  if (splits_out) *splits_out = m.p.splits;
+  if (pages_per_split_out) *pages_per_split_out = m.p.pages_per_split;
+  if (workspace_bytes_out) *workspace_bytes_out = m.p.ws_bytes;
+  return PKV_OK;
+}
+
+pkv_status pkv_paged_attn_decode_multi(const pkv_pool* pool, const void* q, int32_t total_q,
+                                       const int32_t* cu_q, int32_t batch, int32_t num_q_heads,
+                                       const int32_t* block_table, int32_t max_pages,
+                                       const int32_t* seq_lens, int32_t max_q_len,
+                                       int32_t max_seq_len, float softmax_scale,
+                                       int32_t num_splits, void* workspace,
+                                       size_t workspace_bytes, void* out, float* lse,
+                                       void* stream) {
+  pkv_status st = check_pool(pool);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || total_q < 0 || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads ||
+      max_pages <= 0 || max_q_len < 1 || max_seq_len < 0 ||
+      (long long)max_seq_len > (long long)max_pages * pkv::kPageSize || num_splits < 0 ||
+      !std::isfinite(softmax_scale))
+    return PKV_ERR_INVALID;
+  if (pool->dtype != PKV_BF16 || max_q_len > kMultiMaxQ) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0 || total_q == 0) return PKV_OK;
+  if (!q || !cu_q || !block_table || !seq_lens || !out) return PKV_ERR_INVALID;
+  if (!aligned(q, 16) || !aligned(out, 16)) return PKV_ERR_INVALID;
+  const MultiPlan m = make_multi_plan(batch, total_q, num_q_heads, pool->num_kv_heads, max_q_len,
+                                      max_seq_len, num_splits);
+  if (m.p.ws_bytes > 0 &&
+      (!workspace || workspace_bytes < m.p.ws_bytes || !aligned(workspace, 256)))
+    return PKV_ERR_INVALID;
+  if ((long long)batch > 65535 || (long long)pool->num_kv_heads * m.row_groups > 65535 ||
+      (long long)total_q * num_q_heads > 2147483647ll / 2 || m.p.splits > 2147483647 / 2)
+    return PKV_ERR_UNSUPPORTED;
+  pkv_host::MultiLaunch a{};
+  a.k = pool->k;
+  a.v = pool->v;
+  a.num_pages = pool->num_pages;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.q = q;
+  a.total_q = total_q;
+  a.cu_q = cu_q;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.block_table = block_table;
+  a.max_pages = max_pages;
+  a.seq_lens = seq_lens;
+  a.max_q = max_q_len;
+  a.softmax_scale = softmax_scale;
+  a.splits = m.p.splits;
+  a.pages_per_split = m.p.pages_per_split;
+  a.row_groups = m.row_groups;
+  char* base = static_cast<char*>(workspace);
+  a.ws_o = m.p.ws_bytes ? reinterpret_cast<float*>(base + m.p.ws_o_offset) : nullptr;
+  a.ws_lse = m.p.ws_bytes ? reinterpret_cast<float*>(base + m.p.ws_lse_offset) : nullptr;
+  a.out = out;
+  a.lse = lse;
+  return cuda_status(pkv_host::launch_decode_multi(a, static_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_poll_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
   const uint32_t e = pkv_host::take_append_error(s) | pkv_host::take_decode_error(s) |
-                     pkv_host::take_prefill_error(s) | pkv_host::take_qkv_error(s);
+                     pkv_host::take_prefill_error(s) | pkv_host::take_qkv_error(s) |
+                     pkv_host::take_multi_error(s);
   if (e == ~0u) return PKV_ERR_CUDA;
   if (e & pkv::kErrTimeout) return PKV_ERR_TIMEOUT;
   return e ? PKV_ERR_INVALID : PKV_OK;

@@ -165,6 +165,53 @@ __device__ __forceinline__ float fast_log2(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// ------------------------------------------------- split merge
+
+// Log-sum-exp merge of n split partials of one (row, head) by a CTA of
+// exactly 128 threads (thread = channel): lp = their log2-domain lse [n], op = their
+// normalised O [n][128] (written by other CTAs: read through L2).  Block-wide
+// max, weights staged 128 splits at a time in shared memory (wsm, 128
+// floats; red, 4 floats), 8 partial rows in flight per thread.  Every thread
+// of the CTA must call it.  Returns (O, lse2) of channel threadIdx.x; lse2 =
+// -inf and O = 0 when no split holds a key.
+__device__ __forceinline__ float2 merge_splits(const float* lp, const float* op, int n,
+                                               float* wsm, float* red) {
+  const int d = threadIdx.x;
+  float M = -INFINITY;
+  for (int s = d; s < n; s += 128) M = fmaxf(M, __ldcg(lp + s));
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  __syncthreads();                                   // red / wsm free (earlier use done)
+  if ((d & 31) == 0) red[d >> 5] = M;
+  __syncthreads();
+  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  if (M == -INFINITY) return make_float2(0.f, -INFINITY);   // uniform over the CTA
+  float sum = 0.f, O = 0.f;
+  for (int base = 0; base < n; base += 128) {
+    const int cnt = min(128, n - base);
+    __syncthreads();                                 // the previous chunk's weights are used
+    if (d < cnt) wsm[d] = fast_exp2(__ldcg(lp + base + d) - M);
+    __syncthreads();
+    const float* ob = op + (size_t)base * kHeadDim + d;
+    int j = 0;
+    for (; j + 8 <= cnt; j += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(ob + (size_t)(j + u) * kHeadDim);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        sum += wsm[j + u];
+        O += wsm[j + u] * v[u];
+      }
+    }
+    for (; j < cnt; ++j) {
+      sum += wsm[j];
+      O += wsm[j] * __ldcg(ob + (size_t)j * kHeadDim);
+    }
+  }
+  return make_float2(O / sum, M + fast_log2(sum));
+}
+
 }  // namespace pkv
 
 // Host-side helpers shared by the translation units.

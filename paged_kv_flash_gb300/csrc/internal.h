@@ -70,6 +70,35 @@ size_t decode_fixed_scratch_bytes();
 // device with cudaGetSymbolAddress).
 cudaError_t decode_fixed_scratch(void** ptr);
 
+// Split-KV decode of 1..16 query tokens per sequence (decode_multi.cu).
+struct MultiLaunch {
+  const void* k;           // bf16 pool
+  const void* v;
+  int num_pages, num_kv_heads;
+  const void* q;           // bf16 [total_q][Hq][128]
+  int total_q;
+  const int32_t* cu_q;     // [B+1]
+  int batch, num_q_heads;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens; // [B], the step's tokens included
+  int max_q;               // tokens per sequence at most (<= 16)
+  float softmax_scale;
+  int splits, pages_per_split;
+  int row_groups;          // ceil(max_q * G / 64): CTAs per (split, KV head, sequence)
+  float* ws_o;             // [total_q * Hq][splits][128] when splits > 1
+  float* ws_lse;           // [total_q * Hq][splits]
+  void* out;               // bf16 [total_q][Hq][128]
+  float* lse;              // [total_q][Hq] or null
+};
+
+cudaError_t launch_decode_multi(const MultiLaunch& a, cudaStream_t s);
+uint32_t take_multi_error(cudaStream_t s);
+// cuTensorMapEncodeTiled of a bf16 pool (K or V) as 2-D rows of 128
+// channels, one box per 16-row x 64-channel half slab, 128B-swizzled
+// (prefill.cu); `map` points to a CUtensorMap.
+bool encode_bf16_pool_map(void* map, const void* base, int num_pages, int hkv);
+
 struct PrefillLaunch {
   const void* k;
   const void* v;

@@ -1189,6 +1189,10 @@ bool encode_q_map(CUtensorMap* m, const void* q, int total_q, int hq) {
 
 namespace pkv_host {
 
+bool encode_bf16_pool_map(void* map, const void* base, int num_pages, int hkv) {
+  return encode_pool_map(static_cast<CUtensorMap*>(map), base, num_pages, hkv);
+}
+
 // An INT8 pool as a 2-D uint8 tensor of (num_pages * Hkv * 16) rows of 128
 // bytes; a box is one (page, head) slab of 16 rows, 128B-swizzled (the INT8
 // decode kernel reads it).

@@ -54,6 +54,10 @@ SIGNATURES = {
     "pkv_prefill_plan": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "pkv_paged_attn_prefill": (_I, [_POOLP, _P, _I, _P, _I, _I, _P, _I, _P, _I, _F, _P, _SZ, _P,
                                     _P, _P]),
+    "pkv_decode_multi_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I),
+                                   ctypes.POINTER(_I), ctypes.POINTER(_SZ)]),
+    "pkv_paged_attn_decode_multi": (_I, [_POOLP, _P, _I, _P, _I, _I, _P, _I, _P, _I, _I, _F, _I,
+                                         _P, _SZ, _P, _P, _P]),
     "pkv_qkv_norm_rope_append": (_I, [_POOLP, _P, _I, _I, _P, _P, _F, _P, _P, _I, _P, _I, _P,
                                       _I, _P, _P, _P]),
     "pkv_poll_device_error": (_I, [_P]),
@@ -269,6 +273,46 @@ def paged_attn_prefill(pool: Pool, q, cu_q, block_table, seq_lens, max_q_len, so
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
         _stream(stream))
     _check(st, "pkv_paged_attn_prefill")
+    return out, lse
+
+
+def decode_multi_plan(batch, total_q, num_q_heads, num_kv_heads, max_q_len, max_seq_len,
+                      num_splits=0):
+    """(splits, pages_per_split, workspace_bytes) of a multi-token decode."""
+    s, c, w = _I(), _I(), _SZ()
+    st = _lib.pkv_decode_multi_plan(batch, total_q, num_q_heads, num_kv_heads, max_q_len,
+                                    max_seq_len, num_splits, ctypes.byref(s), ctypes.byref(c),
+                                    ctypes.byref(w))
+    _check(st, "pkv_decode_multi_plan")
+    return s.value, c.value, w.value
+
+
+def paged_attn_decode_multi(pool: Pool, q, cu_q, block_table, seq_lens, max_q_len, max_seq_len,
+                            softmax_scale, num_splits=0, workspace=None, out=None, lse=None,
+                            want_lse=True, stream=None):
+    """1..16 query tokens per sequence, causal inside the step (verify steps):
+    q [total_q][Hq][128] bf16 -> (out bf16, lse fp32).  The workspace is
+    allocated when not given."""
+    _need(q, torch.bfloat16, "q")
+    for t, n in ((cu_q, "cu_q"), (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _need(t, torch.int32, n)
+    T, Hq, _ = q.shape
+    B = seq_lens.shape[0]
+    if workspace is None:
+        _, _, wsb = decode_multi_plan(B, T, Hq, pool.k.shape[1], int(max_q_len),
+                                      int(max_seq_len), num_splits)
+        workspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    pc = pool.c()
+    st = _lib.pkv_paged_attn_decode_multi(
+        ctypes.byref(pc), _ptr(q), T, _ptr(cu_q), B, Hq, _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), int(max_q_len), int(max_seq_len), float(softmax_scale), int(num_splits),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
+        _stream(stream))
+    _check(st, "pkv_paged_attn_decode_multi")
     return out, lse
 
 

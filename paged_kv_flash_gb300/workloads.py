@@ -149,6 +149,33 @@ def decode_bf16(rng, lens, Hq, Hkv, slack=0.10, layout=None) -> DecodeCase:
     return DecodeCase(Hq, Hkv, lens, layout, q, k_pool, v_pool)
 
 
+@dataclass
+class MultiCase:
+    """A step of q_lens[b] new tokens per sequence (1..16, e.g. a speculative
+    verify step) over a bf16 cache of seq_lens[b] positions that already holds
+    them; q rows cu_q[b]..cu_q[b+1]-1 belong to sequence b."""
+    Hq: int
+    Hkv: int
+    seq_lens: np.ndarray             # int32 [B]
+    q_lens: np.ndarray               # int32 [B]
+    cu_q: np.ndarray                 # int32 [B+1]
+    layout: Layout
+    q: np.ndarray                    # uint16 bf16 bits [T][Hq][D]
+    k_pool: np.ndarray
+    v_pool: np.ndarray
+    scale: float = 1.0 / np.sqrt(HEAD_DIM)
+
+
+def multi_token_decode(rng, lens, q_lens, Hq, Hkv) -> MultiCase:
+    """Scattered pages filled with N(0,1) K/V for `lens` positions, and
+    N(0,1) queries for the last q_lens[b] positions of each sequence."""
+    dc = decode_bf16(rng, lens, Hq, Hkv)
+    q_lens = np.asarray(q_lens, np.int32)
+    q = normal_bf16(rng, (int(q_lens.sum()), Hq, HEAD_DIM))
+    return MultiCase(Hq, Hkv, dc.seq_lens, q_lens, cu_from_counts(q_lens), dc.layout, q,
+                     dc.k_pool, dc.v_pool)
+
+
 def smoothing_weight(rng) -> np.ndarray:
     """Per-channel key weight w_c ~ U[0.5, 2] (float32), shared by all heads."""
     return rng.uniform(0.5, 2.0, HEAD_DIM).astype(np.float32)

@@ -28,12 +28,12 @@ def check_out(out_gpu: torch.Tensor, ref: np.ndarray, what=""):
     got = host_f32(out_gpu).astype(np.float64)
     assert got.shape == ref.shape, (got.shape, ref.shape)
     err = np.abs(got - ref)
-    bad = err > ATOL + RTOL * np.abs(ref)
+    bad = ~(err <= ATOL + RTOL * np.abs(ref))          # NaN counts as outside
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outputs outside "
                              f"{ATOL}+{RTOL}|ref|; first at {tuple(i)}: got "
-                             f"{got[tuple(i)]}, ref {ref[tuple(i)]}, max err {err.max():.3e}")
+                             f"{got[tuple(i)]}, ref {ref[tuple(i)]}, max err {np.nanmax(err):.3e}")
 
 
 def check_lse(lse_gpu: torch.Tensor, ref: np.ndarray, what=""):

@@ -220,3 +220,42 @@ def test_qkv_prep_rejects_bad_arguments(lib):
     none = list(args)
     none[1] = 0                                       # no tokens: nothing to do
     assert f(ctypes.byref(bf), *none) == 0
+
+
+def test_decode_multi_plan_and_argument_checks(lib):
+    plan = lib.pkv_decode_multi_plan
+    plan.restype = ctypes.c_int32
+    s, c, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    out = (ctypes.byref(s), ctypes.byref(c), ctypes.byref(w))
+    assert plan(2, 20, 8, 2, 16, 1000, 0, *out) == 0
+    assert s.value * c.value * 16 >= 1000 and s.value >= 1
+    assert (w.value == 0) == (s.value == 1)
+    assert plan(2, 20, 8, 2, 16, 1000, 3, *out) == 0 and s.value == 3
+    assert plan(2, 20, 8, 2, 17, 1000, 0, *out) == UNSUPPORTED          # > 16 tokens
+    assert plan(2, 20, 8, 3, 4, 1000, 0, *out) == INVALID               # Hq % Hkv
+    assert plan(2, 20, 8, 2, 0, 1000, 0, *out) == INVALID               # no tokens
+
+    f = lib.pkv_paged_attn_decode_multi
+    f.restype = ctypes.c_int32
+    V = ctypes.c_void_p
+    bf = good_pool()
+    #       q       total cu      B  Hq  bt      maxp sl      maxq maxL scale              splits
+    args = [V(FAKE), 4, V(FAKE), 2, 4, V(FAKE), 4, V(FAKE), 2, 64, ctypes.c_float(0.1), 1,
+            None, 0, V(FAKE), None, None]
+    i8 = good_pool(dtype=1, k_scale=FAKE, v_scale=FAKE)
+    assert f(ctypes.byref(i8), *args) == UNSUPPORTED                    # bf16 pools only
+    bad = list(args)
+    bad[8] = 17                                                         # max_q_len > 16
+    assert f(ctypes.byref(bf), *bad) == UNSUPPORTED
+    bad = list(args)
+    bad[9] = 65                                                         # past the block table
+    assert f(ctypes.byref(bf), *bad) == INVALID
+    bad = list(args)
+    bad[0] = V(FAKE + 4)                                                # unaligned q
+    assert f(ctypes.byref(bf), *bad) == INVALID
+    bad = list(args)
+    bad[11] = 2                                                         # 2 splits, no workspace
+    assert f(ctypes.byref(bf), *bad) == INVALID
+    none = list(args)
+    none[1] = 0                                                         # no tokens
+    assert f(ctypes.byref(bf), *none) == 0
