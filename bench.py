@@ -619,6 +619,22 @@ def profile_case(torch, pk, name, reps=3):
     elif name == "qkv_prep":
         fn, work = qkv_prep_fn(torch, pk, 95)
         unit = "GB/s"
+    elif name == "verify_step":
+        # 8 sequences with 16-token steps at contexts 4k-8k, GQA 32/8
+        lens = rng.integers(4096, 8193, 8)
+        case = W.multi_token_decode(rng, lens, [16] * 8, 32, 8)
+        pool = pk.Pool(to_dev_bf16(torch, case.k_pool), to_dev_bf16(torch, case.v_pool))
+        q, cu = to_dev_bf16(torch, case.q), to_dev(torch, case.cu_q)
+        bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
+        ms = int(lens.max())
+        _, _, wsb = pk.decode_multi_plan(8, len(case.q), 32, 8, 16, ms)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(q)
+        lse = torch.empty((len(case.q), 32), dtype=torch.float32, device="cuda")
+        fn = lambda: pk.paged_attn_decode_multi(pool, q, cu, bt, sl, 16, ms, SCALE, workspace=ws,
+                                                out=out, lse=lse)
+        work = decode_bytes(lens, 8)
+        unit = "GB/s"
     else:
         raise SystemExit(f"unknown profile case {name}")
     for _ in range(reps):
@@ -644,7 +660,7 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["prefill_chunk", "decode_bf16", "decode_int8",
-                                                      "qkv_prep"],
+                                                      "qkv_prep", "verify_step"],
                     help="run one kernel on a fixed workload (for ncu) and exit")
     args = ap.parse_args()
     K, Wu = args.steps, max(3, args.warmup)

@@ -121,8 +121,10 @@ void set_workspace(pkv_host::DecodeLaunch& a, const Plan& p, void* ws, bool fuse
 // page, so a page costs it more as the step grows.  Pages per split: the
 // single-token rule (about 0.8 CTAs per resident slot, 8..128 pages) on
 // three slots per SM, divided by Tp / 2 (at least 4 pages), a multiple of
-// 4.  A GB300 sweep of forced split counts put the optimum there for steps
-// of 1, 8 and 16 tokens.  Workspace: total_q x Hq rows of split partials.
+// 4; a plan between one and two waves of CTAs becomes one wave of longer
+// splits.  A GB300 sweep of forced split counts put the optimum there for
+// steps of 1, 8 and 16 tokens.  Workspace: total_q x Hq rows of split
+// partials.
 constexpr int kMultiMaxQ = 16;
 constexpr int kMultiRowsPerCta = 64;
 constexpr int kMultiCtasPerSm = 3;
@@ -153,6 +155,14 @@ MultiPlan make_multi_plan(int batch, int total_q, int num_q_heads, int num_kv_he
     c = std::max<long long>(4, c / std::max(1, Tp / 2));
     c = (c + 3) / 4 * 4;
     C = (int)std::min<long long>(c, mp);
+    // between one and two waves of CTAs: take one wave of longer splits
+    // (the second, partial wave would leave most SMs idle)
+    const long long ctas = units * ((mp + C - 1) / C);
+    if (ctas > slots && ctas < 2 * slots && units <= slots) {
+      const long long s1 = slots / units;                     // splits that fit one wave
+      const long long c1 = (mp + s1 - 1) / s1;
+      if (c1 <= kPlanMaxPages) C = (int)std::min<long long>(c1, mp);
+    }
   }
   C = std::max(1, C);
   Plan& p = m.p;
