@@ -189,23 +189,24 @@ class Mixed:
         self.out_d = torch.empty((self.R, wl.Hq, D), dtype=torch.bfloat16, device="cuda")
         self.lse_d = torch.empty((self.R, wl.Hq), dtype=torch.float32, device="cuda")
 
-    def step(self, i, ev=None, inputs=None):
+    def step(self, i, ev=None, inputs=None, outs=None):
         """Step i (chunk i mod 14).  ev: list of 3 event pairs to record
         (append, prefill, decode) or None.  inputs: per-step device tensors
-        that replace the resident ones (end-to-end path)."""
+        that replace the resident ones (end-to-end path); outs: (out_p,
+        lse_p, out_d, lse_d) to write instead of the resident outputs."""
         pk, wl = self.pk, self.wl
         st = self.steps[i % len(self.steps)]
         x = inputs or st
+        out_p, lse_p, out_d, lse_d = outs or (self.out_p, self.lse_p, self.out_d, self.lse_d)
         n = st["chunk_len"]
         if ev: ev[0].record()
         pk.kv_append(self.pool, x["k_new"], x["v_new"], st["cu_app"], self.bt_all, st["lens_app"])
         if ev: ev[1].record()
         pk.paged_attn_prefill(self.pool, x["q_chunk"], st["cu_q"], self.bt_prompt, st["lens_p"],
-                              n, SCALE, workspace=self.ws_p, out=self.out_p[:n],
-                              lse=self.lse_p[:n])
+                              n, SCALE, workspace=self.ws_p, out=out_p[:n], lse=lse_p[:n])
         if ev: ev[2].record()
         pk.paged_attn_decode(self.pool, x["q_dec"], self.bt_dec, st["lens_d"], st["max_dec"],
-                             SCALE, workspace=self.ws, out=self.out_d, lse=self.lse_d)
+                             SCALE, workspace=self.ws, out=out_d, lse=lse_d)
         if ev: ev[3].record()
 
 
@@ -274,47 +275,79 @@ def time_mixed(torch, pk, mixed, K, Wu, world, rank):
 
 def time_e2e(torch, pk, mixed, K):
     """Same steps through the public API from pinned host buffers: every step
-    copies its inputs host->device and reads its outputs back."""
+    copies its inputs host->device and reads its outputs back.  The copies
+    overlap the kernels, as a serving loop would run them: step i+1's inputs
+    go up on one copy stream while step i computes, and step i's outputs come
+    back on another from one of two output buffers (the compute stream waits
+    for a buffer's read-back before reusing it)."""
     host = []
     for st in mixed.steps:
         s = st["host"]
         host.append(dict(k_new=pinned_bf16(torch, s.k_new), v_new=pinned_bf16(torch, s.v_new),
                          q_chunk=pinned_bf16(torch, s.q_chunk),
                          q_dec=pinned_bf16(torch, s.q_decode)))
-    dev = [dict((k, torch.empty_like(v, device="cuda")) for k, v in h.items()) for h in host]
-    T = mixed.out_p.shape[0]
-    out_h = torch.empty(mixed.out_p.shape, dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty(mixed.lse_p.shape, dtype=torch.float32).pin_memory()
-    outd_h = torch.empty(mixed.out_d.shape, dtype=torch.bfloat16).pin_memory()
-    lsed_h = torch.empty(mixed.lse_d.shape, dtype=torch.float32).pin_memory()
     nsteps = len(mixed.steps)
-    h2d = d2h = 0
+    dev = [dict((k, torch.empty_like(v, device="cuda")) for k, v in h.items()) for h in host]
+    outs = [(mixed.out_p, mixed.lse_p, mixed.out_d, mixed.lse_d),
+            tuple(torch.empty_like(t) for t in (mixed.out_p, mixed.lse_p, mixed.out_d,
+                                                 mixed.lse_d))]
+    host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[0])
+    compute = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(nsteps)]       # inputs of chunk j are on the device
+    ev_used = [torch.cuda.Event() for _ in range(nsteps)]     # step using chunk j's inputs is done
+    ev_done = [torch.cuda.Event() for _ in range(2)]          # step writing output buffer b is done
+    ev_back = [torch.cuda.Event() for _ in range(2)]          # output buffer b has been read back
+    counts = {"h2d": 0, "d2h": 0}
+    used = [False] * nsteps
+    back = [False, False]
 
-    def one(i):
-        nonlocal h2d, d2h
+    def upload(i):
         j = i % nsteps
-        for k, v in host[j].items():
-            dev[j][k].copy_(v, non_blocking=True)
-            h2d += v.numel() * v.element_size()
-        mixed.step(i, inputs=dev[j])
-        n = mixed.steps[j]["chunk_len"]
-        out_h[:n].copy_(mixed.out_p[:n], non_blocking=True)
-        lse_h[:n].copy_(mixed.lse_p[:n], non_blocking=True)
-        outd_h.copy_(mixed.out_d, non_blocking=True)
-        lsed_h.copy_(mixed.lse_d, non_blocking=True)
-        d2h += (n * mixed.out_p.shape[1] * D * 2 + n * mixed.lse_p.shape[1] * 4 +
-                outd_h.numel() * 2 + lsed_h.numel() * 4)
+        with torch.cuda.stream(up):
+            if used[j]:
+                up.wait_event(ev_used[j])
+            for k, v in host[j].items():
+                dev[j][k].copy_(v, non_blocking=True)
+                counts["h2d"] += v.numel() * v.element_size()
+            ev_in[j].record(up)
 
-    for i in range(nsteps):
-        one(i)
-    torch.cuda.synchronize()
-    h2d = d2h = 0
+    def run(i):
+        j, b = i % nsteps, i % 2
+        compute.wait_event(ev_in[j])
+        if back[b]:
+            compute.wait_event(ev_back[b])
+        mixed.step(i, inputs=dev[j], outs=outs[b])
+        ev_used[j].record(compute)
+        used[j] = True
+        ev_done[b].record(compute)
+        n = mixed.steps[j]["chunk_len"]
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[b])
+            op, lp, od, ld = outs[b]
+            host_out[0][:n].copy_(op[:n], non_blocking=True)
+            host_out[1][:n].copy_(lp[:n], non_blocking=True)
+            host_out[2].copy_(od, non_blocking=True)
+            host_out[3].copy_(ld, non_blocking=True)
+            ev_back[b].record(down)
+        back[b] = True
+        counts["d2h"] += (n * op.shape[1] * D * 2 + n * lp.shape[1] * 4 + od.numel() * 2 +
+                          ld.numel() * 4)
+
+    def loop(n_iter):
+        upload(0)
+        for i in range(n_iter):
+            if i + 1 < n_iter:
+                upload(i + 1)
+            run(i)
+        torch.cuda.synchronize()
+
+    loop(nsteps)                                   # warm-up pass over every chunk
+    counts["h2d"] = counts["d2h"] = 0
     t0 = time.perf_counter()
-    for i in range(K):
-        one(i)
-    torch.cuda.synchronize()
+    loop(K)
     dt = time.perf_counter() - t0
-    return dt * 1e6 / K, h2d // K, d2h // K
+    return dt * 1e6 / K, counts["h2d"] // K, counts["d2h"] // K
 
 
 # ------------------------------------------------------ other workloads
