@@ -167,22 +167,26 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // ------------------------------------------------- split merge
 
-// Log-sum-exp merge of n split partials of one (row, head) by a CTA of
-// exactly 128 threads (thread = channel): lp = their log2-domain lse [n], op = their
-// normalised O [n][128] (written by other CTAs: read through L2).  Block-wide
-// max, weights staged 128 splits at a time in shared memory (wsm, 128
-// floats; red, 4 floats), 8 partial rows in flight per thread.  Every thread
-// of the CTA must call it.  Returns (O, lse2) of channel threadIdx.x; lse2 =
-// -inf and O = 0 when no split holds a key.
+// Log-sum-exp merge of n split partials of one (row, head) by a CTA of 128
+// or more threads; threads 0..127 take one channel each, the others only
+// join the barriers.  lp = the partials' log2-domain lse [n], op = their
+// normalised O [n][128] (written by other CTAs: read through L2).
+// Block-wide max, weights staged 128 splits at a time in shared memory
+// (wsm, 128 floats; red, 4 floats), 8 partial rows in flight per thread.
+// Every thread of the CTA must call it.  Returns (O, lse2) of channel
+// threadIdx.x (threads 0..127); lse2 = -inf and O = 0 when no split holds a
+// key.
 __device__ __forceinline__ float2 merge_splits(const float* lp, const float* op, int n,
                                                float* wsm, float* red) {
   const int d = threadIdx.x;
+  const bool act = d < 128;
   float M = -INFINITY;
-  for (int s = d; s < n; s += 128) M = fmaxf(M, __ldcg(lp + s));
+  if (act)
+    for (int s = d; s < n; s += 128) M = fmaxf(M, __ldcg(lp + s));
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   __syncthreads();                                   // red / wsm free (earlier use done)
-  if ((d & 31) == 0) red[d >> 5] = M;
+  if (act && (d & 31) == 0) red[d >> 5] = M;
   __syncthreads();
   M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   if (M == -INFINITY) return make_float2(0.f, -INFINITY);   // uniform over the CTA
@@ -192,6 +196,7 @@ __device__ __forceinline__ float2 merge_splits(const float* lp, const float* op,
     __syncthreads();                                 // the previous chunk's weights are used
     if (d < cnt) wsm[d] = fast_exp2(__ldcg(lp + base + d) - M);
     __syncthreads();
+    if (!act) continue;
     const float* ob = op + (size_t)base * kHeadDim + d;
     int j = 0;
     for (; j + 8 <= cnt; j += 8) {
@@ -209,7 +214,7 @@ __device__ __forceinline__ float2 merge_splits(const float* lp, const float* op,
       O += wsm[j] * __ldcg(ob + (size_t)j * kHeadDim);
     }
   }
-  return make_float2(O / sum, M + fast_log2(sum));
+  return act ? make_float2(O / sum, M + fast_log2(sum)) : make_float2(0.f, -INFINITY);
 }
 
 }  // namespace pkv

@@ -202,11 +202,10 @@ __device__ __forceinline__ void process_page(WarpState<G>& st, const uint8_t* bu
 // domain, O unnormalised); combine them, then write the bf16 output (one
 // split) or the split's partial, and with FUSED let the last split of the
 // (sequence, KV head) merge the partials.
-template <int G, bool FUSED>
+template <int G, bool FUSED, int W = pkv_host::kDecodeWarps>
 __device__ __forceinline__ void merge_warps(const pkv_host::DecodeLaunch& a, uint8_t* smem,
                                             const uint8_t* bufs, size_t warp_stride, int split,
                                             int h, int b, int nv, bool direct) {
-  constexpr int W = pkv_host::kDecodeWarps;
   const int Hq = a.num_q_heads;
   for (int t = threadIdx.x; t < G * kHeadDim; t += W * 32) {
     const int g = t / kHeadDim, d = t % kHeadDim;
@@ -248,7 +247,7 @@ __device__ __forceinline__ void merge_warps(const pkv_host::DecodeLaunch& a, uin
   // the flag sits in the unused end of the barrier header (no static shared
   // memory: it would pad the 1024-byte aligned dynamic allocation)
   volatile uint32_t& s_last = *reinterpret_cast<volatile uint32_t*>(smem + 1020);
-  static_assert(pkv_host::kDecodeWarps * 5 * 8 <= 1020, "barrier header");
+  static_assert(W * 5 * 8 <= 1020, "barrier header");
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t* ctr = a.ws_ctr + (size_t)b * a.num_kv_heads + h;
@@ -272,8 +271,10 @@ __device__ __forceinline__ void merge_warps(const pkv_host::DecodeLaunch& a, uin
     const float2 r = merge_splits(a.ws_lse + bh * a.splits, a.ws_o + bh * a.splits * kHeadDim,
                                   nv, wsm, red);
     const int d = threadIdx.x;
-    static_cast<__nv_bfloat16*>(a.out)[bh * kHeadDim + d] = __float2bfloat16_rn(r.x);
-    if (a.lse && d == 0) a.lse[bh] = r.y * kLn2;
+    if (d < kHeadDim) {
+      static_cast<__nv_bfloat16*>(a.out)[bh * kHeadDim + d] = __float2bfloat16_rn(r.x);
+      if (a.lse && d == 0) a.lse[bh] = r.y * kLn2;
+    }
   }
 }
 
@@ -511,12 +512,13 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
 // every fragment load conflict-free.
 namespace i8mma {
 
+constexpr int W = 8;                                    // warps per CTA, pages round-robin
 constexpr int NB = 3;                                   // page buffers per warp
 constexpr int SLAB = kPageSize * kHeadDim;              // 2 KiB: K or V of one (page, head)
 constexpr int KV = 2 * SLAB;                            // one page buffer (1 KiB aligned)
 constexpr int SC = 2 * kPageSize * 4;                   // K and V scales of one page
 constexpr int WARP_BYTES = NB * KV;
-constexpr int SMEM = 1024 + pkv_host::kDecodeWarps * NB * (KV + SC);
+constexpr int SMEM = 1024 + W * NB * (KV + SC);
 constexpr uint32_t kMagic = 0x64646464u;                // f16 exponent byte of 1024
 constexpr uint32_t kBias2 = 0x64806480u;                // f16x2 (1152, 1152)
 constexpr float kBias = 1152.0f;
@@ -575,12 +577,11 @@ __device__ __forceinline__ void tma_slab(uint32_t dst, const CUtensorMap* map, i
 }  // namespace i8mma
 
 template <int G, bool FUSED>
-__global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32, 4)
+__global__ void __launch_bounds__(i8mma::W * 32, 2)
     decode_split_i8mma_kernel(const __grid_constant__ CUtensorMap tk,
                               const __grid_constant__ CUtensorMap tv,
                               const __grid_constant__ pkv_host::DecodeLaunch a) {
   using namespace i8mma;
-  constexpr int W = pkv_host::kDecodeWarps;
   constexpr uint32_t FULL = 0xffffffffu;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -859,7 +860,7 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32, 4)
     wl[r] = failed ? 0.f : l;
   }
   __syncthreads();
-  merge_warps<G, FUSED>(a, smem, bufs, (size_t)WARP_BYTES, split, h, b, nv, direct);
+  merge_warps<G, FUSED, W>(a, smem, bufs, (size_t)WARP_BYTES, split, h, b, nv, direct);
 }
 
 // Combine (separate kernel): out = sum_s 2^(lse_s - lse) * O_s, lse = log2
@@ -920,7 +921,7 @@ cudaError_t launch_i8mma_as(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   dim3 grid(a.splits, a.num_kv_heads, a.batch);
   decode_split_i8mma_kernel<G, FUSED>
-      <<<grid, pkv_host::kDecodeWarps * 32, i8mma::SMEM, s>>>(tk, tv, a);
+      <<<grid, i8mma::W * 32, i8mma::SMEM, s>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
