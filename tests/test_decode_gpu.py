@@ -204,3 +204,26 @@ def test_fused_decode_workspace_reuse_is_exact():
             assert torch.equal(o, o0) and torch.equal(l, l0)
             assert int(ws[:zero].count_nonzero()) == 0
     assert pk.poll_device_error() == pk.OK
+
+
+def test_int8_empty_context_and_single_keys(pk):
+    """INT8 rows with no cached position (out 0, lse -inf), one key, one page
+    exactly, and one key into the next page, through the tensor-core path."""
+    rng = np.random.default_rng(60)
+    lens = np.array([0, 1, 16, 17], np.int32)
+    layout = W.scatter_pages(rng, lens)
+    T = int(lens.sum())
+    w = W.smoothing_weight(rng)
+    app = W.AppendCase(2, W.cu_from_counts(lens), lens, layout,
+                       W.keys_with_channel_weight(rng, (T, 2, W.HEAD_DIM), w),
+                       W.normal_bf16(rng, (T, 2, W.HEAD_DIM)), k_smooth=w)
+    pools = oracle.kv_append_int8(*W.empty_pool_int8(layout.num_pages, 2), app.k_new,
+                                  app.v_new, app.cu_new, layout.block_table, lens, k_smooth=w)
+    q = W.normal_bf16(rng, (4, 8, W.HEAD_DIM))
+    case = W.DecodeCase(8, 2, lens, layout, q, None, None)
+    ro, rl = oracle_decode(case, int8_pools=pools, smooth=w)
+    assert np.isneginf(rl[0]).all() and (ro[0] == 0).all()
+    for splits in (0, 2):
+        out, lse = gpu_decode(pk, case, splits, int8_pools=pools, smooth=w)
+        check_out(out, ro, f"int8 edge splits={splits}")
+        check_lse(lse, rl, f"int8 edge splits={splits}")

@@ -99,3 +99,16 @@ def test_sequence_longer_than_max_q_is_flagged(pk):
     gpu_multi(pk, case, max_q=4)                 # sequence 1 has 5 tokens
     assert pk.poll_device_error() == pk.ERR_INVALID
     assert pk.poll_device_error() == pk.OK
+
+
+def test_sequence_without_tokens_in_the_step(pk):
+    """A batch where the middle sequence has no token in this step (an empty
+    cu_q range): its cache is not read and the others are unaffected."""
+    rng = np.random.default_rng(314)
+    case = W.multi_token_decode(rng, [300, 500, 64], [3, 0, 5], Hq=8, Hkv=2)
+    ro, rl = oracle_multi(case)
+    for splits in (0, 3):
+        out, lse = gpu_multi(pk, case, splits)
+        assert pk.poll_device_error() == pk.OK
+        check_out(out, ro, f"empty step splits={splits}")
+        check_lse(lse, rl, f"empty step splits={splits}")
