@@ -62,12 +62,14 @@ __global__ void __launch_bounds__(256) append_bf16_kernel(pkv_host::AppendLaunch
     const long long row = i >> 4;                 // (token, head)
     const int h = (int)(row % a.num_kv_heads);
     const int t = (int)(row / a.num_kv_heads);
+    // the new vectors need nothing from the slot lookup: load them first, so
+    // that their latency overlaps the lookup's chain of dependent loads
+    const uint4 kx = __ldg(kn + i);
+    const uint4 vx = __ldg(vn + i);
     const long long fs = slot_of_row(a, t);
     if (fs < 0) continue;
     const long long page = fs >> 4, slot = fs & 15;
     const long long dst = (((page * a.num_kv_heads + h) << 4) + slot) * 16 + c;
-    const uint4 kx = __ldg(kn + i);
-    const uint4 vx = __ldg(vn + i);
     kp[dst] = kx;
     vp[dst] = vx;
   }
@@ -110,12 +112,12 @@ __global__ void __launch_bounds__(256) append_int8_kernel(pkv_host::AppendLaunch
        row += nwarps) {
     const int h = (int)(row % a.num_kv_heads);
     const int t = (int)(row / a.num_kv_heads);
+    const uint2 kr = __ldg(kn + row * 32 + lane);     // before the slot lookup (see above)
+    const uint2 vr = __ldg(vn + row * 32 + lane);
     const long long fs = slot_of_row(a, t);
     if (fs < 0) continue;
     const long long page = fs >> 4, slot = fs & 15;
     const long long dst = ((page * a.num_kv_heads + h) << 4) + slot;   // vector index
-    const uint2 kr = __ldg(kn + row * 32 + lane);
-    const uint2 vr = __ldg(vn + row * 32 + lane);
     float k0 = bf16lo(kr.x), k1 = bf16hi(kr.x), k2 = bf16lo(kr.y), k3 = bf16hi(kr.y);
     if (a.k_smooth) {
       k0 = __fdiv_rn(k0, w.x);
