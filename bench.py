@@ -210,6 +210,18 @@ class Mixed:
         if ev: ev[3].record()
 
 
+def max_over_ranks(torch, x):
+    """The largest x over the ranks of the default process group (x itself
+    without one): the job's time is its slowest replica's."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def time_mixed(torch, pk, mixed, K, Wu, world, rank):
     dist = torch.distributed if world > 1 else None
     for i in range(Wu):
@@ -234,11 +246,7 @@ def time_mixed(torch, pk, mixed, K, Wu, world, rank):
         dist.barrier()
     clk = clocks.stop()
     assert pk.poll_device_error() == pk.OK, "device-side error in the timed region"
-    total_ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(torch, t0.elapsed_time(t1))
     app_ms = pre_ms = dec_ms = 0.0
     flops = dbytes = 0.0
     launches = 0
@@ -684,7 +692,7 @@ def profile_case(torch, pk, name, reps=3):
 
 # ---------------------------------------------------------------- main
 
-def main():
+def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1400)
@@ -695,7 +703,7 @@ def main():
     ap.add_argument("--profile-case", choices=["prefill_chunk", "decode_bf16", "decode_int8",
                                                       "qkv_prep", "verify_step"],
                     help="run one kernel on a fixed workload (for ncu) and exit")
-    args = ap.parse_args()
+    args = ap.parse_args(argv)
     K, Wu = args.steps, max(3, args.warmup)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
