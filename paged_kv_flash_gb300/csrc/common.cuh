@@ -1,7 +1,8 @@
 // common.cuh -- device helpers shared by the sm_103a kernels of libpagedkv.
 //
 // Everything here is plain PTX for sm_103a: mbarriers with bounded waits,
-// bulk (TMA-engine) copies, bf16/int8 unpacking and packed f32x2 arithmetic.
+// bulk (TMA-engine) copies, bf16 unpacking, packed f32x2 arithmetic and the
+// log-sum-exp merge of split partials.
 #pragma once
 
 #include <cstdint>
@@ -110,13 +111,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Signed byte i (0..3) of a word -> fp32, exactly: the byte (offset by 128)
-// becomes the low mantissa bits of 2^23, then the bias is subtracted.
-template <int I>
-__device__ __forceinline__ uint32_t i8_biased_bits(uint32_t w_xor80) {
-  return __byte_perm(w_xor80, 0x4B000000u, 0x7540u + I);
-}
-constexpr float kI8Bias = 8388736.0f;  // 2^23 + 128
 
 // ------------------------------------------------- packed f32x2 helpers
 

@@ -62,10 +62,6 @@ struct Cfg {
   static_assert(BUF % 128 == 0, "page buffers stay 128-byte aligned");
 };
 
-struct SplitArgs {
-  pkv_host::DecodeLaunch a;
-};
-
 // Loads 8 consecutive bf16 at a shared address as four fp32 pairs.
 __device__ __forceinline__ void load_widen(const uint8_t* p, float2 (&x)[4]) {
   const uint4 r = *reinterpret_cast<const uint4*>(p);
