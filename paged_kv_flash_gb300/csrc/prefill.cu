@@ -779,7 +779,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // QK_B(j), and the other way round.  QK_x(j) overwrites S_x, which holds
     // P_x(j-1): it is issued after PV_x(j-1), and MMAs of one thread run in
     // issue order.  A segment's first QKs only touch S, so they overlap the
-    // previous segment's epilogue, which reads O.
+    // previous segment's epilogue, which reads O.  K(j) is waited for only
+    // after PV_A(j-1) is issued: that PV does not need it and runs while K
+    // lands.
     bool ok = true;
     int t = 0, cnt_a = 0, cnt_b = 0;
     for (int sg = 0;; ++sg) {
@@ -804,7 +806,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool has_qk = j < j1;
         const int tt = t + (j - j0);              // global block index of block j
         const int st = tt % NSTAGE, pst = (tt + NSTAGE - 1) % NSTAGE;
-        if (has_qk && !(ok = wait_bar(bar(BAR_KF + st), (tt / NSTAGE) & 1, abort_flag))) break;
+        bool k_ready = false;                     // K(j) is waited for only before the first QK
         if (j > j0) {
           if (!(ok = wait_bar(bar(BAR_VF + pst), ((tt - 1) / NSTAGE) & 1, abort_flag))) break;
           const int kbase = (j - 1) * BN;
@@ -838,6 +840,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
           }
           if (has_qk && j < jex) {
+            if (!k_ready) {
+              if (!(ok = wait_bar(bar(BAR_KF + st), (tt / NSTAGE) & 1, abort_flag))) break;
+              k_ready = true;
+            }
             tc_fence_after();
             if (lane == 0) {
               const uint32_t q_s = base_s + OFF_Q + x * TILE, k_s = base_s + OFF_K + st * TILE;
@@ -850,7 +856,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         if (lane == 0) {
-          if (has_qk) mma_commit(bar(BAR_KE + st));
+          if (k_ready) mma_commit(bar(BAR_KE + st));
           if (j > j0) mma_commit(bar(BAR_VE + pst));
         }
         __syncwarp();
