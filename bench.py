@@ -427,6 +427,7 @@ def other_configs(torch, pk, hbm, bf16):
             r["graph_note"] = "back-to-back launches in one CUDA graph, warm L2"
         res[name] = r
         assert pk.poll_device_error() == pk.OK
+        return out
 
     c1 = W.decode_1k()
     p1 = pk.Pool(to_dev_bf16(torch, c1.k_pool), to_dev_bf16(torch, c1.v_pool))
@@ -438,14 +439,31 @@ def other_configs(torch, pk, hbm, bf16):
     decode_entry("batched_decode_b64_gqa32x8_fused", c3, p3, 512, fused=True)
     del c3, p3
     for B in (1, 8):
+        # The same keys and values in a bf16 pool and in INT8 pools with and
+        # without key smoothing; the bf16 decode's output is the reference
+        # the quantisation error is measured against.
         app, q = W.int8_long_decode(B=B)
-        pool = pk.Pool.empty(app.layout.num_pages, app.Hkv, dtype=torch.int8)
-        pk.kv_append(pool, to_dev_bf16(torch, app.k_new), to_dev_bf16(torch, app.v_new),
-                     to_dev(torch, app.cu_new), to_dev(torch, app.layout.block_table),
-                     to_dev(torch, app.seq_lens), k_smooth=to_dev(torch, app.k_smooth))
         case = W.DecodeCase(32, app.Hkv, app.seq_lens, app.layout, q, None, None)
-        decode_entry(f"int8_decode_32k_b{B}", case, pool, 264, smooth=app.k_smooth)
-        del pool
+        kn, vn = to_dev_bf16(torch, app.k_new), to_dev_bf16(torch, app.v_new)
+        cu, btd, sld = (to_dev(torch, app.cu_new), to_dev(torch, app.layout.block_table),
+                        to_dev(torch, app.seq_lens))
+        pb = pk.Pool.empty(app.layout.num_pages, app.Hkv)
+        pk.kv_append(pb, kn, vn, cu, btd, sld)
+        ref = decode_entry(f"bf16_decode_32k_b{B}", case, pb, 512).float()
+        del pb
+        for smooth in (True, False):
+            pool = pk.Pool.empty(app.layout.num_pages, app.Hkv, dtype=torch.int8)
+            w = app.k_smooth if smooth else None
+            pk.kv_append(pool, kn, vn, cu, btd, sld,
+                         k_smooth=to_dev(torch, w) if w is not None else None)
+            name = f"int8_decode_32k_b{B}" + ("" if smooth else "_no_smoothing")
+            o = decode_entry(name, case, pool, 264, smooth=w).float()
+            res[name]["rel_l2_err_vs_bf16_decode"] = float(
+                f"{((o - ref).norm() / ref.norm()).item():.3g}")
+            res[name]["max_abs_err_vs_bf16_decode"] = float(f"{(o - ref).abs().max().item():.3g}")
+            res[name]["key_smoothing"] = smooth
+            del pool
+        del kn, vn
     # 1,024-token prompt: append + prefill
     app, q = W.prefill_prompt()
     pool = pk.Pool.empty(app.layout.num_pages, app.Hkv)

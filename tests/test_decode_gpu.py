@@ -149,6 +149,28 @@ def test_int8_32k_batch8_sampled(pk):
     check_lse(lse[idx], rl, "int8 32k b8")
 
 
+def test_int8_key_smoothing_reduces_the_error_against_exact_attention(pk):
+    """Keys whose channels carry scales w_c ~ U[0.5, 2] lose less to the INT8
+    cache when they are quantised divided by w (the key smoothing of the
+    "INT8 KV cache" section): at 32,768 positions the GPU's INT8 decode with
+    smoothing is closer to the exact attention over the unquantised bf16
+    keys and values (fp64 oracle) than without.  Both stay within the
+    decode tolerance of it."""
+    app, q = W.int8_long_decode(B=1)
+    kp, vp = W.empty_pool_bf16(app.layout.num_pages, app.Hkv)
+    kp, vp = oracle.kv_append_bf16(kp, vp, app.k_new, app.v_new, app.cu_new,
+                                   app.layout.block_table, app.seq_lens)
+    exact, _ = oracle_decode(W.DecodeCase(32, app.Hkv, app.seq_lens, app.layout, q, kp, vp))
+    err = {}
+    for smooth in (True, False):
+        case, pools, w = int8_case(pk, 1, smooth)
+        out, _ = gpu_decode(pk, case, int8_pools=pools, smooth=w)
+        check_out(out, exact, f"int8 32k smooth={smooth} against unquantised K/V")
+        o = out.float().cpu().numpy().astype(np.float64)
+        err[smooth] = np.linalg.norm(o - exact) / np.linalg.norm(exact)
+    assert err[True] < 0.95 * err[False], err
+
+
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
 def test_int8_group_sizes_ragged(pk, G):
     rng = np.random.default_rng(50 + G)
