@@ -28,6 +28,18 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Sequence b that owns packed row t of a batch whose rows are laid out by
+// prefix sums cu[0..batch] (cu non-decreasing, cu[0] = 0): the last b with
+// cu[b] <= t, by binary search.
+__device__ __forceinline__ int owner_seq(const int32_t* __restrict__ cu, int batch, int t) {
+  int lo = 0, hi = batch;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -215,5 +227,17 @@ __device__ __forceinline__ float2 merge_splits(const float* lp, const float* op,
 
 // Host-side helpers shared by the translation units.
 namespace pkv_host {
+
+// Reads a translation unit's device error word (its address is passed, from
+// that unit) and clears it when it is set; ~0 if the copy fails.
+inline uint32_t take_error_word(const void* symbol, cudaStream_t s) {
+  uint32_t h = 0, zero = 0;
+  if (cudaMemcpyFromSymbolAsync(&h, symbol, sizeof h, 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return ~0u;
+  cudaStreamSynchronize(s);
+  if (h) cudaMemcpyToSymbolAsync(symbol, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
+  cudaStreamSynchronize(s);
+  return h;
+}
 int sm_count();                 // cached SM count of the current device
 }

@@ -960,16 +960,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, bool int8, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-uint32_t take_decode_error(cudaStream_t s) {
-  uint32_t h = 0, zero = 0;
-  if (cudaMemcpyFromSymbolAsync(&h, g_err_decode, sizeof h, 0, cudaMemcpyDeviceToHost, s) !=
-      cudaSuccess)
-    return ~0u;
-  cudaStreamSynchronize(s);
-  if (h) cudaMemcpyToSymbolAsync(g_err_decode, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
-  cudaStreamSynchronize(s);
-  return h;
-}
+uint32_t take_decode_error(cudaStream_t s) { return take_error_word(&g_err_decode, s); }
 
 }  // namespace pkv_host
 

@@ -102,15 +102,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
   }
 }
 
-__device__ __forceinline__ int owner_seq(const int32_t* __restrict__ cu, int batch, int t) {
-  int lo = 0, hi = batch;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 __global__ void __launch_bounds__(kThreads, 3)
     decode_multi_kernel(const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv,
@@ -494,15 +485,6 @@ cudaError_t launch_decode_multi(const MultiLaunch& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-uint32_t take_multi_error(cudaStream_t s) {
-  uint32_t h = 0, zero = 0;
-  if (cudaMemcpyFromSymbolAsync(&h, g_err_multi, sizeof h, 0, cudaMemcpyDeviceToHost, s) !=
-      cudaSuccess)
-    return ~0u;
-  cudaStreamSynchronize(s);
-  if (h) cudaMemcpyToSymbolAsync(g_err_multi, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
-  cudaStreamSynchronize(s);
-  return h;
-}
+uint32_t take_multi_error(cudaStream_t s) { return take_error_word(&g_err_multi, s); }
 
 }  // namespace pkv_host

@@ -21,20 +21,10 @@ using namespace pkv;
 
 __device__ uint32_t g_err_append;
 
-// Sequence b that owns new row t: cu[b] <= t < cu[b+1] (cu non-decreasing).
-__device__ __forceinline__ int owner(const int32_t* __restrict__ cu, int batch, int t) {
-  int lo = 0, hi = batch;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 // Flat slot (page * 16 + slot) of new row t, or -1 (and the error word set)
 // when the position or the page id falls outside the caller's arrays.
 __device__ __forceinline__ long long slot_of_row(const pkv_host::AppendLaunch& a, int t) {
-  const int b = owner(a.cu_new, a.batch, t);
+  const int b = owner_seq(a.cu_new, a.batch, t);
   const int first = __ldg(a.cu_new + b);
   const int n = __ldg(a.cu_new + b + 1) - first;
   const int p = __ldg(a.seq_lens + b) - n + (t - first);
@@ -152,15 +142,6 @@ cudaError_t launch_append(const AppendLaunch& a, bool int8, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-uint32_t take_append_error(cudaStream_t s) {
-  uint32_t h = 0, zero = 0;
-  if (cudaMemcpyFromSymbolAsync(&h, g_err_append, sizeof h, 0, cudaMemcpyDeviceToHost, s) !=
-      cudaSuccess)
-    return ~0u;
-  cudaStreamSynchronize(s);
-  if (h) cudaMemcpyToSymbolAsync(g_err_append, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
-  cudaStreamSynchronize(s);
-  return h;
-}
+uint32_t take_append_error(cudaStream_t s) { return take_error_word(&g_err_append, s); }
 
 }  // namespace pkv_host

@@ -1259,15 +1259,6 @@ size_t prefill_workspace_bytes(int ctas) {
 
 size_t prefill_workspace_zero_bytes(int ctas) { return ws_counter_bytes(ctas); }
 
-uint32_t take_prefill_error(cudaStream_t s) {
-  uint32_t h = 0, zero = 0;
-  if (cudaMemcpyFromSymbolAsync(&h, g_err_prefill, sizeof h, 0, cudaMemcpyDeviceToHost, s) !=
-      cudaSuccess)
-    return ~0u;
-  cudaStreamSynchronize(s);
-  if (h) cudaMemcpyToSymbolAsync(g_err_prefill, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
-  cudaStreamSynchronize(s);
-  return h;
-}
+uint32_t take_prefill_error(cudaStream_t s) { return take_error_word(&g_err_prefill, s); }
 
 }  // namespace pkv_host

@@ -27,15 +27,6 @@ using namespace pkv;
 
 __device__ uint32_t g_err_qkv;
 
-__device__ __forceinline__ int owner_seq(const int32_t* __restrict__ cu, int batch, int t) {
-  int lo = 0, hi = batch;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(cu + mid) <= t) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 __device__ __forceinline__ uint32_t bf16x2_rn(float2 v) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(v.y), "f"(v.x));
@@ -204,15 +195,6 @@ cudaError_t launch_qkv_prep(const QkvPrepLaunch& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-uint32_t take_qkv_error(cudaStream_t s) {
-  uint32_t h = 0, zero = 0;
-  if (cudaMemcpyFromSymbolAsync(&h, g_err_qkv, sizeof h, 0, cudaMemcpyDeviceToHost, s) !=
-      cudaSuccess)
-    return ~0u;
-  cudaStreamSynchronize(s);
-  if (h) cudaMemcpyToSymbolAsync(g_err_qkv, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s);
-  cudaStreamSynchronize(s);
-  return h;
-}
+uint32_t take_qkv_error(cudaStream_t s) { return take_error_word(&g_err_qkv, s); }
 
 }  // namespace pkv_host
