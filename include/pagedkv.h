@@ -345,6 +345,17 @@ pkv_status pkv_qkv_norm_rope_append(const pkv_pool* pool, const void* qkv, int32
  */
 pkv_status pkv_poll_device_error(void* stream);
 
+/*
+ * Self-test of the error path of the kernels' bounded waits: one device
+ * thread waits, with the bounded wait a prefill CTA uses before it merges a
+ * unit cut between CTAs, until the uint32 at `counter` (device memory, the
+ * caller's, only read) reaches `target`.  If nothing raises it, the wait
+ * gives up after one second, the next pkv_poll_device_error reports
+ * PKV_ERR_TIMEOUT, and the context stays usable.  Asynchronous on `stream`;
+ * PKV_ERR_INVALID for a NULL counter.
+ */
+pkv_status pkv_selftest_bounded_wait(const uint32_t* counter, uint32_t target, void* stream);
+
 /* Static text for a status code. */
 const char* pkv_status_string(pkv_status status);
 

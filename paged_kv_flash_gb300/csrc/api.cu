@@ -486,6 +486,12 @@ pkv_status pkv_paged_attn_decode_multi(const pkv_pool* pool, const void* q, int3
   return cuda_status(pkv_host::launch_decode_multi(a, static_cast<cudaStream_t>(stream)));
 }
 
+pkv_status pkv_selftest_bounded_wait(const uint32_t* counter, uint32_t target, void* stream) {
+  if (!counter) return PKV_ERR_INVALID;
+  return cuda_status(
+      pkv_host::launch_wait_selftest(counter, target, static_cast<cudaStream_t>(stream)));
+}
+
 pkv_status pkv_poll_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return PKV_ERR_CUDA;
@@ -503,7 +509,7 @@ const char* pkv_status_string(pkv_status s) {
     case PKV_ERR_INVALID: return "invalid argument";
     case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
     case PKV_ERR_CUDA: return "CUDA error";
-    case PKV_ERR_TIMEOUT: return "device-side wait timed out or device-side check failed";
+    case PKV_ERR_TIMEOUT: return "a device-side bounded wait ran out";
   }
   return "unknown status";
 }

@@ -130,6 +130,8 @@ size_t prefill_workspace_zero_bytes(int ctas);
 int prefill_ctas(int sms);
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s);
 uint32_t take_prefill_error(cudaStream_t s);
+// One thread waits (bounded, as a merging prefill CTA does) for *counter >= target.
+cudaError_t launch_wait_selftest(const uint32_t* counter, uint32_t target, cudaStream_t s);
 
 struct QkvPrepLaunch {
   const void* qkv;         // bf16 [T][Hq + 2 Hkv][128]

@@ -1191,9 +1191,22 @@ bool encode_q_map(CUtensorMap* m, const void* q, int total_q, int hq) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Self-test of the bounded-wait error path: one thread waits, with the wait
+// a merging CTA uses, for a counter that nothing will raise.
+__global__ void bounded_wait_selftest_kernel(const uint32_t* ctr, uint32_t target) {
+  __shared__ uint32_t abort_flag;
+  abort_flag = 0u;
+  (void)wait_count(ctr, target, &abort_flag);
+}
+
 }  // namespace
 
 namespace pkv_host {
+
+cudaError_t launch_wait_selftest(const uint32_t* counter, uint32_t target, cudaStream_t s) {
+  bounded_wait_selftest_kernel<<<1, 1, 0, s>>>(counter, target);
+  return cudaGetLastError();
+}
 
 bool encode_bf16_pool_map(void* map, const void* base, int num_pages, int hkv) {
   return encode_pool_map(static_cast<CUtensorMap*>(map), base, num_pages, hkv);

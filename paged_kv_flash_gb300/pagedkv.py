@@ -60,6 +60,7 @@ SIGNATURES = {
                                          _P, _SZ, _P, _P, _P]),
     "pkv_qkv_norm_rope_append": (_I, [_POOLP, _P, _I, _I, _P, _P, _F, _P, _P, _I, _P, _I, _P,
                                       _I, _P, _P, _P]),
+    "pkv_selftest_bounded_wait": (_I, [_P, ctypes.c_uint32, _P]),
     "pkv_poll_device_error": (_I, [_P]),
     "pkv_status_string": (ctypes.c_char_p, [_I]),
     "pkv_device_sm_count": (_I, []),
@@ -340,6 +341,15 @@ def qkv_norm_rope_append(pool: Pool, qkv, num_q_heads, cu_new, block_table, seq_
         _ptr(q_out), _stream(stream))
     _check(st, "pkv_qkv_norm_rope_append")
     return q_out
+
+
+def selftest_bounded_wait(counter, target, stream=None):
+    """One device thread waits (bounded, one second) for the int32 tensor
+    `counter` (read as uint32) to reach `target`; a wait that runs out shows
+    as ERR_TIMEOUT at the next poll_device_error."""
+    _need(counter, torch.int32, "counter")
+    _check(_lib.pkv_selftest_bounded_wait(_ptr(counter), int(target), _stream(stream)),
+           "pkv_selftest_bounded_wait")
 
 
 def poll_device_error(stream=None) -> int:

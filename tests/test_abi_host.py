@@ -259,3 +259,8 @@ def test_decode_multi_plan_and_argument_checks(lib):
     none = list(args)
     none[1] = 0                                                         # no tokens
     assert f(ctypes.byref(bf), *none) == 0
+
+
+def test_wait_selftest_rejects_a_null_counter(lib):
+    """Checked on the host before any launch (no GPU needed)."""
+    assert lib.pkv_selftest_bounded_wait(None, 1, None) == -1

@@ -54,6 +54,22 @@ def test_tiny_causal_brute_force(pk):
     check_lse(lse, rl, "tiny causal")
 
 
+def test_a_bounded_wait_that_runs_out_reports_timeout_and_the_context_stays_usable(pk):
+    """The bounded wait a merging CTA uses, on a counter that nothing raises:
+    it gives up after about a second, the poll reports the timeout once, a
+    reached target returns at once, and the next prefill is still correct."""
+    import time
+    ctr = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.monotonic()
+    pk.selftest_bounded_wait(ctr, 1)
+    assert pk.poll_device_error() == pk.ERR_TIMEOUT
+    assert 0.9 < time.monotonic() - t0 < 60
+    assert pk.poll_device_error() == pk.OK        # the word is cleared once read
+    pk.selftest_bounded_wait(ctr, 0)              # already reached: no wait, no error
+    assert pk.poll_device_error() == pk.OK
+    test_tiny_causal_brute_force(pk)
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (4, 4), (16, 2)])
 def test_ragged_chunks_against_prefix(pk, Hq, Hkv):
     """Chunks spanning several 128-row tiles and 128-key blocks, ragged tails."""
