@@ -529,12 +529,17 @@ def verify_entry(torch, pk, rng, lens, qlens, flush, hbm, bf16, Hq=32, Hkv=8):
     assert pk.poll_device_error() == pk.OK
     byts = decode_bytes(lens, Hkv)
     fl = sum(prefill_flops(qn, L, Hq) for qn, L in zip(qlens, lens))
-    return {"us": round(m_med, 2), "us_min": round(m_min, 2), "GBps": round(byts / m_med / 1e3, 1),
-            "frac_of_measured": round(byts / m_med / 1e3 / hbm, 4), "bytes": int(byts),
-            "TFLOPs": round(fl / m_med / 1e6, 1), "splits": S,
-            "prefill_kernel_us": round(p_med, 2),
-            "note": ("multi-token decode (pkv_paged_attn_decode_multi): split kernel + combine; "
-                     "prefill_kernel_us = the same step through pkv_paged_attn_prefill")}
+    r = {"us": round(m_med, 2), "us_min": round(m_min, 2), "GBps": round(byts / m_med / 1e3, 1),
+         "frac_of_measured": round(byts / m_med / 1e3 / hbm, 4), "bytes": int(byts),
+         "TFLOPs": round(fl / m_med / 1e6, 1), "splits": S,
+         "prefill_kernel_us": round(p_med, 2),
+         "note": ("multi-token decode (pkv_paged_attn_decode_multi): split kernel + combine; "
+                  "prefill_kernel_us = the same step through pkv_paged_attn_prefill")}
+    if byts < 64 * 2**20:                         # small steps are launch- and latency-bound
+        r["graph_us_per_launch"] = round(time_graph(torch, fm), 2)
+        r["graph_prefill_kernel_us_per_launch"] = round(time_graph(torch, fp), 2)
+        r["graph_note"] = "back-to-back launches in one CUDA graph, warm L2"
+    return r
 
 
 def qkv_prep_fn(torch, pk, seed, T=2048, L=16384, Hq=32, Hkv=8):
