@@ -62,9 +62,13 @@ constexpr int NUM_THREADS = 320;              // softmax A: warps 0-3, B: 4-7, T
 // pipeline fill and drain, epilogue), and each CTA gets at least kMinCost.
 constexpr int kUnitCost0 = 4;
 constexpr int kMinCost = 2 * kUnitCost0;
-// Below this much work per CTA, cutting units costs more (storing and
-// merging parts) than it saves, and CTAs take whole units instead.
+// CTAs cut units (split mode) when they have at least this much work each,
+// or when whole units would leave the largest one more than kSplitGain
+// above an even share (few, long units: a short chunk against a long
+// context); otherwise cutting costs more (storing and merging parts) than it
+// saves and CTAs take whole units.
 constexpr int kSplitMinPerCta = 96;
+constexpr int kSplitGain = 24;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
 // TMEM columns: S_A 0..127, S_B 128..255, O_A 256..383, O_B 384..511.  P of a
@@ -381,7 +385,8 @@ __device__ __forceinline__ long long muldiv(long long a, long long b, long long 
   return (long long)(p / (unsigned long long)c);
 }
 
-__device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, int b) {
+// Cost of sequence b's units (all heads); umax: the largest unit's cost so far.
+__device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, int b, int& umax) {
   const int q0 = a.cu_q[b];
   const int q_len = a.cu_q[b + 1] - q0;
   const int L = a.seq_lens[b];
@@ -390,7 +395,11 @@ __device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, 
     return 0;
   }
   long long c = 0;
-  for (int p = 0; p < n_pairs_of(q_len); ++p) c += unit_cost(pair_geom(q0, q_len, L, p));
+  for (int p = 0; p < n_pairs_of(q_len); ++p) {
+    const int u = unit_cost(pair_geom(q0, q_len, L, p));
+    c += u;
+    umax = max(umax, u);
+  }
   return c * a.num_q_heads;
 }
 
@@ -404,12 +413,18 @@ struct Cursor {
 
 __device__ __forceinline__ int pair_of(const Cursor& c) { return n_pairs_of(c.g.q_len) - 1 - c.pi; }
 
-// Total cost W, by one warp (every lane gets it).
-__device__ __forceinline__ long long total_cost(const pkv_host::PrefillLaunch& a, int lane) {
+// Total cost W and the largest unit's cost, by one warp (every lane gets
+// both).
+__device__ __forceinline__ long long total_cost(const pkv_host::PrefillLaunch& a, int lane,
+                                                int& umax) {
   long long t = 0;
-  for (int b = lane; b < a.batch; b += 32) t += seq_cost(a, b);
+  umax = 0;
+  for (int b = lane; b < a.batch; b += 32) t += seq_cost(a, b, umax);
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  for (int o = 16; o >= 1; o >>= 1) {
+    t += __shfl_xor_sync(0xffffffffu, t, o);
+    umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, o));
+  }
   return t;
 }
 
@@ -482,7 +497,8 @@ __device__ __forceinline__ Cursor locate_unit(const pkv_host::PrefillLaunch& a, 
   long long sb = 0;
   for (int b0 = 0; b0 < a.batch; b0 += 32) {
     const int b = b0 + lane;
-    const long long cst = b < a.batch ? seq_cost(a, b) : 0;
+    int unused = 0;
+    const long long cst = b < a.batch ? seq_cost(a, b, unused) : 0;
     long long incl = cst;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -583,8 +599,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the first block's page ids of the first sequence: usually needed first
     if (lane < BN / kPageSize && lane < a.max_pages)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + lane));
-    W = total_cost(a, lane);
-    split = W >= (long long)kSplitMinPerCta * P;
+    int umax = 0;
+    W = total_cost(a, lane, umax);
+    split = W >= (long long)kSplitMinPerCta * P ||
+            (long long)umax * P > W + (long long)kSplitGain * P;
     Pe = split ? active_ctas(W, P) : P;
     if (split && cta < Pe) {
       lo = range_lo(W, Pe, cta);

@@ -70,6 +70,20 @@ def test_a_bounded_wait_that_runs_out_reports_timeout_and_the_context_stays_usab
     test_tiny_causal_brute_force(pk)
 
 
+def test_short_chunk_over_long_context_cuts_units(pk):
+    """A 300-row chunk against 6,000 cached positions, GQA 32/8: 64 long units
+    for more CTAs than that, so the work is cut between CTAs and the parts
+    merged, although each CTA's share is small."""
+    rng = np.random.default_rng(66)
+    case, q, cu, mq = chunk_case(rng, [(300, 6000)], Hq=32, Hkv=8)
+    out, lse = run(pk, case, q, cu, mq)
+    rows = np.r_[0:8, 120:136, 250:300].astype(np.int32)   # both tiles, both pairs, the tail
+    ro, rl = ref(case, q, cu, rows=rows)
+    idx = torch.from_numpy(rows).long().cuda()
+    check_out(out[idx], ro, "short chunk over a long context")
+    check_lse(lse[idx], rl, "short chunk over a long context")
+
+
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (4, 4), (16, 2)])
 def test_ragged_chunks_against_prefix(pk, Hq, Hkv):
     """Chunks spanning several 128-row tiles and 128-key blocks, ragged tails."""
