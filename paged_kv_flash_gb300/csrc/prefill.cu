@@ -62,12 +62,10 @@ constexpr int NUM_THREADS = 320;              // softmax A: warps 0-3, B: 4-7, T
 // pipeline fill and drain, epilogue), and each CTA gets at least kMinCost.
 constexpr int kUnitCost0 = 4;
 constexpr int kMinCost = 2 * kUnitCost0;
-// CTAs cut units (split mode) when they have at least this much work each,
-// or when whole units would leave the largest one more than kSplitGain
-// above an even share (few, long units: a short chunk against a long
-// context); otherwise cutting costs more (storing and merging parts) than it
-// saves and CTAs take whole units.
-constexpr int kSplitMinPerCta = 96;
+// CTAs cut units (split mode) when whole units would finish later than an
+// even share plus kSplitGain, the cost of storing and merging cut parts.
+// Whole units end no earlier than the largest unit, nor than ceil(units / P)
+// units of average cost on the most loaded CTA.
 constexpr int kSplitGain = 24;
 constexpr int WARP_TMA = 8, WARP_MMA = 9;
 constexpr uint32_t TMEM_COLS = 512;
@@ -322,6 +320,10 @@ __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target,
 // cf .. cl; and since kMinCost exceeds the largest gap between block starts
 // (kUnitCost0 + 2), every active CTA has work.
 //
+// Whether units are cut at all follows from W, the largest unit and the
+// number of units (kSplitGain above); when they are not, CTAs take whole
+// units in a snake order.
+//
 // Each CTA walks its range backwards (units from its last position down),
 // so that for a unit cut between CTAs the part in CTA cl (the unit's last
 // blocks) is the last segment cl runs, while the part in any lower CTA k is
@@ -385,8 +387,10 @@ __device__ __forceinline__ long long muldiv(long long a, long long b, long long 
   return (long long)(p / (unsigned long long)c);
 }
 
-// Cost of sequence b's units (all heads); umax: the largest unit's cost so far.
-__device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, int b, int& umax) {
+// Cost of sequence b's units (all heads); umax: the largest unit's cost so
+// far; nunits: units so far.
+__device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, int b, int& umax,
+                                              long long& nunits) {
   const int q0 = a.cu_q[b];
   const int q_len = a.cu_q[b + 1] - q0;
   const int L = a.seq_lens[b];
@@ -400,6 +404,7 @@ __device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, 
     c += u;
     umax = max(umax, u);
   }
+  nunits += (long long)n_pairs_of(q_len) * a.num_q_heads;
   return c * a.num_q_heads;
 }
 
@@ -413,17 +418,19 @@ struct Cursor {
 
 __device__ __forceinline__ int pair_of(const Cursor& c) { return n_pairs_of(c.g.q_len) - 1 - c.pi; }
 
-// Total cost W and the largest unit's cost, by one warp (every lane gets
-// both).
+// Total cost W, the largest unit's cost and the number of units, by one
+// warp (every lane gets all three).
 __device__ __forceinline__ long long total_cost(const pkv_host::PrefillLaunch& a, int lane,
-                                                int& umax) {
+                                                int& umax, long long& nunits) {
   long long t = 0;
   umax = 0;
-  for (int b = lane; b < a.batch; b += 32) t += seq_cost(a, b, umax);
+  nunits = 0;
+  for (int b = lane; b < a.batch; b += 32) t += seq_cost(a, b, umax, nunits);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     t += __shfl_xor_sync(0xffffffffu, t, o);
     umax = max(umax, __shfl_xor_sync(0xffffffffu, umax, o));
+    nunits += __shfl_xor_sync(0xffffffffu, nunits, o);
   }
   return t;
 }
@@ -497,8 +504,9 @@ __device__ __forceinline__ Cursor locate_unit(const pkv_host::PrefillLaunch& a, 
   long long sb = 0;
   for (int b0 = 0; b0 < a.batch; b0 += 32) {
     const int b = b0 + lane;
-    int unused = 0;
-    const long long cst = b < a.batch ? seq_cost(a, b, unused) : 0;
+    int um = 0;
+    long long nu = 0;
+    const long long cst = b < a.batch ? seq_cost(a, b, um, nu) : 0;
     long long incl = cst;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -600,9 +608,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane < BN / kPageSize && lane < a.max_pages)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + lane));
     int umax = 0;
-    W = total_cost(a, lane, umax);
-    split = W >= (long long)kSplitMinPerCta * P ||
-            (long long)umax * P > W + (long long)kSplitGain * P;
+    long long units = 0;
+    W = total_cost(a, lane, umax, units);
+    if (units > 0) {
+      // whole units' makespan vs the split share, both times units * P
+      const long long per = (units + P - 1) / P;
+      const long long whole = max((long long)umax * units * P, per * W * P);
+      split = whole > (W + (long long)kSplitGain * P) * units;
+    }
     Pe = split ? active_ctas(W, P) : P;
     if (split && cta < Pe) {
       lo = range_lo(W, Pe, cta);
