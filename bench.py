@@ -489,6 +489,25 @@ def other_configs(torch, pk, hbm, bf16):
         "append_us": round(a_med, 2), "append_GBps": round(2 * 2 * 1024 * 8 * 256 / a_med / 1e3, 1)}
     assert pk.poll_device_error() == pk.OK
     del pool
+    # short chunks against a long cached context (chunked prefill of a long
+    # prompt in 512-row chunks): few long units, cut between CTAs
+    for qn, L in ((512, 8192), (128, 32768)):
+        c = W.decode_bf16(np.random.default_rng(1007), [L], 32, 8)
+        pool = pk.Pool(to_dev_bf16(torch, c.k_pool), to_dev_bf16(torch, c.v_pool))
+        qc = to_dev_bf16(torch, W.normal_bf16(np.random.default_rng(1008), (qn, 32, D)))
+        cuc, btc, slc = (to_dev(torch, W.cu_from_counts([qn])),
+                         to_dev(torch, c.layout.block_table), to_dev(torch, c.seq_lens))
+        oc = torch.empty_like(qc)
+        lc = torch.empty((qn, 32), dtype=torch.float32, device="cuda")
+        pc = lambda: pk.paged_attn_prefill(pool, qc, cuc, btc, slc, qn, SCALE, workspace=ws_p,
+                                           out=oc, lse=lc)
+        med, mn = time_events(torch, pc, flush=flush)
+        fl = prefill_flops(qn, L, 32)
+        res[f"prefill_chunk{qn}_ctx{L}_gqa32x8"] = {
+            "us": round(med, 2), "us_min": round(mn, 2), "TFLOPs": round(fl / med / 1e6, 1),
+            "frac_of_measured_burst": round(fl / med / 1e6 / bf16, 4), "flops": fl}
+        assert pk.poll_device_error() == pk.OK
+        del pool, c
     # verify steps (multi-token decode), with the prefill kernel on the same step
     rng = np.random.default_rng(1006)
     for name, lens, qlens in (("verify_16tok_1k_b1_gqa32x8", [1024], [16]),

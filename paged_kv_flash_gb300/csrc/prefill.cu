@@ -310,6 +310,11 @@ __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target,
 // block (tile A needs blocks 0 .. nblk_a-1, tile B 0 .. nblk_b-1; nblk_b is
 // nblk_a or nblk_a + 1, or 0 when the pair's second tile is past the chunk),
 // plus kUnitCost0 in front of block 0 for starting and finishing the unit.
+// When the second tile is past the chunk (a chunk of at most 128 rows, or
+// its odd last tile) and the query heads of a KV head come in pairs (G
+// even), the unit instead holds the same rows for heads 2u and 2u + 1, which
+// read the same K/V: tile B is the next head, not the next 128 rows, and the
+// pair has Hq / 2 units.
 // Units are ordered by sequence, pairs from the last (heaviest) down, heads
 // innermost (the query heads of a KV head are neighbours, so they share K/V
 // through L2).  The total cost W is cut into Pe equal ranges, one per active
@@ -338,6 +343,7 @@ __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target,
 struct PairGeom {
   int q0, q_len, L, row0, rows_a, rows_b, pmin_a, nblk_a, nblk_b, nblk;
   int nd;                       // blocks both tiles need (cost 2 each); the rest cost 1
+  int hpu;                      // heads per unit: 1 (tile B = next rows), 2 (= next head)
 };
 
 __device__ __forceinline__ bool seq_valid(const pkv_host::PrefillLaunch& a, int q0, int q_len,
@@ -348,7 +354,12 @@ __device__ __forceinline__ bool seq_valid(const pkv_host::PrefillLaunch& a, int 
 
 __device__ __forceinline__ int n_pairs_of(int q_len) { return (q_len + 2 * BM - 1) / (2 * BM); }
 
-__device__ __forceinline__ PairGeom pair_geom(int q0, int q_len, int L, int p) {
+// The query heads of a KV head come in pairs (G even): units may pair heads.
+__device__ __forceinline__ bool heads_pair(const pkv_host::PrefillLaunch& a) {
+  return (a.num_q_heads / a.num_kv_heads) % 2 == 0;
+}
+
+__device__ __forceinline__ PairGeom pair_geom(int q0, int q_len, int L, int p, bool hp) {
   PairGeom g;
   g.q0 = q0;
   g.q_len = q_len;
@@ -356,9 +367,14 @@ __device__ __forceinline__ PairGeom pair_geom(int q0, int q_len, int L, int p) {
   g.row0 = p * 2 * BM;
   g.rows_a = max(0, min(BM, q_len - g.row0));
   g.rows_b = max(0, min(BM, q_len - g.row0 - BM));
+  g.hpu = 1;
+  if (hp && g.rows_b == 0 && g.rows_a > 0) {     // tile B: the same rows, the next head
+    g.hpu = 2;
+    g.rows_b = g.rows_a;
+  }
   g.pmin_a = L - q_len + g.row0;
   g.nblk_a = g.rows_a > 0 ? (g.pmin_a + g.rows_a - 1) / BN + 1 : 0;
-  g.nblk_b = g.rows_b > 0 ? (g.pmin_a + BM + g.rows_b - 1) / BN + 1 : 0;
+  g.nblk_b = g.rows_b > 0 ? (g.pmin_a + (g.hpu == 2 ? 0 : BM) + g.rows_b - 1) / BN + 1 : 0;
   g.nblk = max(g.nblk_a, g.nblk_b);
   g.nd = min(g.nblk_a, g.nblk_b);
   return g;
@@ -366,6 +382,10 @@ __device__ __forceinline__ PairGeom pair_geom(int q0, int q_len, int L, int p) {
 
 __device__ __forceinline__ int unit_cost(const PairGeom& g) {
   return kUnitCost0 + g.nblk_a + g.nblk_b;
+}
+// units of a pair of row tiles: one per head, or per head pair
+__device__ __forceinline__ int units_of(const pkv_host::PrefillLaunch& a, const PairGeom& g) {
+  return a.num_q_heads / g.hpu;
 }
 // cost offset of block j within its unit (the unit's fixed cost comes first)
 __device__ __forceinline__ int block_off(const PairGeom& g, int j) {
@@ -390,7 +410,7 @@ __device__ __forceinline__ long long muldiv(long long a, long long b, long long 
 // Cost of sequence b's units (all heads); umax: the largest unit's cost so
 // far; nunits: units so far.
 __device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, int b, int& umax,
-                                              long long& nunits) {
+                                              long long& nunits, bool hp) {
   const int q0 = a.cu_q[b];
   const int q_len = a.cu_q[b + 1] - q0;
   const int L = a.seq_lens[b];
@@ -400,15 +420,17 @@ __device__ __forceinline__ long long seq_cost(const pkv_host::PrefillLaunch& a, 
   }
   long long c = 0;
   for (int p = 0; p < n_pairs_of(q_len); ++p) {
-    const int u = unit_cost(pair_geom(q0, q_len, L, p));
-    c += u;
+    const PairGeom g = pair_geom(q0, q_len, L, p, hp);
+    const int u = unit_cost(g);
+    c += (long long)u * units_of(a, g);
+    nunits += units_of(a, g);
     umax = max(umax, u);
   }
-  nunits += (long long)n_pairs_of(q_len) * a.num_q_heads;
-  return c * a.num_q_heads;
+  return c;
 }
 
-// Position of the work walk: unit (b, pair index pi, head hq).
+// Position of the work walk: unit (b, pair index pi, unit hq of the pair:
+// query head hq, or heads 2 hq and 2 hq + 1 when g.hpu == 2).
 struct Cursor {
   int b, pi, hq;
   long long ustart;             // cost position of the unit's first block
@@ -421,11 +443,11 @@ __device__ __forceinline__ int pair_of(const Cursor& c) { return n_pairs_of(c.g.
 // Total cost W, the largest unit's cost and the number of units, by one
 // warp (every lane gets all three).
 __device__ __forceinline__ long long total_cost(const pkv_host::PrefillLaunch& a, int lane,
-                                                int& umax, long long& nunits) {
+                                                int& umax, long long& nunits, bool hp) {
   long long t = 0;
   umax = 0;
   nunits = 0;
-  for (int b = lane; b < a.batch; b += 32) t += seq_cost(a, b, umax, nunits);
+  for (int b = lane; b < a.batch; b += 32) t += seq_cost(a, b, umax, nunits, hp);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) {
     t += __shfl_xor_sync(0xffffffffu, t, o);
@@ -436,16 +458,16 @@ __device__ __forceinline__ long long total_cost(const pkv_host::PrefillLaunch& a
 }
 
 // The unit before the cursor's unit (end if none).
-__device__ __forceinline__ void prev_unit(const pkv_host::PrefillLaunch& a, Cursor& c) {
+__device__ __forceinline__ void prev_unit(const pkv_host::PrefillLaunch& a, Cursor& c, bool hp) {
   if (c.hq > 0) {
     --c.hq;
     c.ustart -= unit_cost(c.g);
     return;
   }
-  c.hq = a.num_q_heads - 1;
   if (c.pi > 0) {
     --c.pi;
-    c.g = pair_geom(c.g.q0, c.g.q_len, c.g.L, pair_of(c));
+    c.g = pair_geom(c.g.q0, c.g.q_len, c.g.L, pair_of(c), hp);
+    c.hq = units_of(a, c.g) - 1;
     c.ustart -= unit_cost(c.g);
     return;
   }
@@ -454,7 +476,8 @@ __device__ __forceinline__ void prev_unit(const pkv_host::PrefillLaunch& a, Curs
     if (!seq_valid(a, q0, q_len, L) || q_len == 0) continue;
     c.b = b;
     c.pi = n_pairs_of(q_len) - 1;
-    c.g = pair_geom(q0, q_len, L, 0);
+    c.g = pair_geom(q0, q_len, L, 0, hp);
+    c.hq = units_of(a, c.g) - 1;
     c.ustart -= unit_cost(c.g);
     return;
   }
@@ -462,9 +485,10 @@ __device__ __forceinline__ void prev_unit(const pkv_host::PrefillLaunch& a, Curs
 }
 
 // Moves the cursor n units forward (end if there are fewer).
-__device__ __forceinline__ void skip_units(const pkv_host::PrefillLaunch& a, Cursor& c, int n) {
+__device__ __forceinline__ void skip_units(const pkv_host::PrefillLaunch& a, Cursor& c, int n,
+                                           bool hp) {
   while (n > 0 && !c.end) {
-    const int left = a.num_q_heads - c.hq;        // units left in this pair, this one included
+    const int left = units_of(a, c.g) - c.hq;     // units left in this pair, this one included
     if (n < left) {
       c.hq += n;
       c.ustart += (long long)n * unit_cost(c.g);
@@ -475,7 +499,7 @@ __device__ __forceinline__ void skip_units(const pkv_host::PrefillLaunch& a, Cur
     c.hq = 0;
     if (c.pi + 1 < n_pairs_of(c.g.q_len)) {
       ++c.pi;
-      c.g = pair_geom(c.g.q0, c.g.q_len, c.g.L, pair_of(c));
+      c.g = pair_geom(c.g.q0, c.g.q_len, c.g.L, pair_of(c), hp);
       continue;
     }
     int b = c.b + 1;
@@ -484,7 +508,7 @@ __device__ __forceinline__ void skip_units(const pkv_host::PrefillLaunch& a, Cur
       if (!seq_valid(a, q0, q_len, L) || q_len == 0) continue;
       c.b = b;
       c.pi = 0;
-      c.g = pair_geom(q0, q_len, L, n_pairs_of(q_len) - 1);
+      c.g = pair_geom(q0, q_len, L, n_pairs_of(q_len) - 1, hp);
       break;
     }
     if (b >= a.batch) c.end = true;
@@ -494,7 +518,8 @@ __device__ __forceinline__ void skip_units(const pkv_host::PrefillLaunch& a, Cur
 // Cursor at the unit whose cost range holds pos (0 <= pos < W), by one warp
 // (every lane gets the same cursor).
 __device__ __forceinline__ Cursor locate_unit(const pkv_host::PrefillLaunch& a, long long pos,
-                                              int lane) {
+                                              int lane,
+                                              bool hp) {
   Cursor c;
   c.end = true;
   c.b = c.pi = c.hq = 0;
@@ -506,7 +531,7 @@ __device__ __forceinline__ Cursor locate_unit(const pkv_host::PrefillLaunch& a, 
     const int b = b0 + lane;
     int um = 0;
     long long nu = 0;
-    const long long cst = b < a.batch ? seq_cost(a, b, um, nu) : 0;
+    const long long cst = b < a.batch ? seq_cost(a, b, um, nu, hp) : 0;
     long long incl = cst;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -528,8 +553,8 @@ __device__ __forceinline__ Cursor locate_unit(const pkv_host::PrefillLaunch& a, 
   long long p0 = sb;
   const int np = n_pairs_of(q_len);
   for (int pi = 0; pi < np; ++pi) {
-    const PairGeom g = pair_geom(q0, q_len, L, np - 1 - pi);
-    const long long cbp = (long long)unit_cost(g) * a.num_q_heads;
+    const PairGeom g = pair_geom(q0, q_len, L, np - 1 - pi, hp);
+    const long long cbp = (long long)unit_cost(g) * units_of(a, g);
     if (pos < p0 + cbp) {
       c.b = bf;
       c.pi = pi;
@@ -563,7 +588,7 @@ struct SegDesc {
   int j0, j1;                   // blocks of this segment
   int cf, nown;                 // CTAs holding parts of the unit; nown == 1: all here
   int end;                      // no further segment
-  int pad[3];
+  int pmin_b, qrow_b, hq_b;     // tile B: first position, q row, head
 };
 static_assert(sizeof(SegDesc) == 64, "descriptor slot size");
 
@@ -574,6 +599,7 @@ struct PrefillParams {
   float4* ws_o;                 // [P slots][2 tiles][32 channel quads][128 rows] normalised O
 };
 
+template <bool HP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                    const __grid_constant__ CUtensorMap tq, const __grid_constant__ PrefillParams prm) {
@@ -599,7 +625,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // 2P+c, ... (heaviest first, snaking so that the CTAs that took the
   // heaviest units of one round take the lightest of the next).
   long long W = 0, lo = 0, hi = 0;
-  bool split = false;
+  bool split = false, hp = false;           // hp: units pair heads (HP builds only)
   int Pe = P;
   Cursor c;
   c.end = true;
@@ -607,25 +633,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the first block's page ids of the first sequence: usually needed first
     if (lane < BN / kPageSize && lane < a.max_pages)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + lane));
+    // whole units' makespan vs the split share (both times units * P)
+    auto cut = [&](long long w, int um, long long n) {
+      const long long per = (n + P - 1) / P;
+      return n > 0 && max((long long)um * n * P, per * w * P) > (w + (long long)kSplitGain * P) * n;
+    };
     int umax = 0;
     long long units = 0;
-    W = total_cost(a, lane, umax, units);
-    if (units > 0) {
-      // whole units' makespan vs the split share, both times units * P
-      const long long per = (units + P - 1) / P;
-      const long long whole = max((long long)umax * units * P, per * W * P);
-      split = whole > (W + (long long)kSplitGain * P) * units;
+    if (HP && heads_pair(a)) {
+      // Pair heads unless whole units of single heads would already leave
+      // CTAs idle (then pairs would halve the CTAs at work).
+      W = total_cost(a, lane, umax, units, false);
+      hp = cut(W, umax, units) || units > P;
     }
+    W = total_cost(a, lane, umax, units, hp);
+    split = cut(W, umax, units);
     Pe = split ? active_ctas(W, P) : P;
     if (split && cta < Pe) {
       lo = range_lo(W, Pe, cta);
       hi = range_lo(W, Pe, cta + 1);
     }
     if (split) {
-      if (lo < hi) c = locate_unit(a, hi - 1, lane);
+      if (lo < hi) c = locate_unit(a, hi - 1, lane, hp);
     } else if (W > 0) {
-      c = locate_unit(a, 0, lane);
-      skip_units(a, c, cta);
+      c = locate_unit(a, 0, lane, hp);
+      skip_units(a, c, cta, hp);
     }
   }
 
@@ -676,7 +708,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           j1 = first_block_at(c.g, hi - c.ustart);
           if (j0 < j1) break;
           if (c.ustart <= lo) c.end = true;
-          else prev_unit(a, c);
+          else prev_unit(a, c, hp);
         }
         if (!c.end) {
           cf = owner_of(W, Pe, c.ustart + block_off(c.g, 0));
@@ -694,7 +726,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         d.end = has ? 0 : 1;
         if (has) {
           d.qrow0 = c.g.q0 + c.g.row0;
-          d.hq = c.hq;
+          if (HP) {
+            d.hq = c.hq * c.g.hpu;                // tile A's head
+            // tile B: the next 128 rows, or (head pair) the same rows, next head
+            d.pmin_b = c.g.pmin_a + (c.g.hpu == 2 ? 0 : BM);
+            d.qrow_b = d.qrow0 + (c.g.hpu == 2 ? 0 : BM);
+            d.hq_b = d.hq + (c.g.hpu == 2 ? 1 : 0);
+          } else {
+            d.hq = c.hq;
+          }
           d.L = c.g.L;
           d.pmin_a = c.g.pmin_a;
           d.rows_a = c.g.rows_a;
@@ -711,7 +751,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (!has) break;
 
-      const int hkv = c.hq / G;
+      const int hkv = (HP ? c.hq * c.g.hpu : c.hq) / G;   // a head pair shares it
       const int npages = (c.g.L + kPageSize - 1) / kPageSize;
       const int32_t* bt_row = a.block_table + (size_t)c.b * a.max_pages;
       // Page ids of block j, one per lane 0..7 (0 past the sequence's pages).
@@ -774,11 +814,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (rows > 0) {
               // rows past the end of q read as zeros; rows of the next
               // sequence only feed padding rows, whose results are never stored
-              const int row = c.g.q0 + c.g.row0 + x * BM;
+              // tile B: the next 128 rows of the head, or (head pair) the
+              // same rows of the next head
+              const int row = c.g.q0 + c.g.row0 + (HP && c.g.hpu == 2 ? 0 : x * BM);
+              const int head = HP ? c.hq * c.g.hpu + (c.g.hpu == 2 ? x : 0) : c.hq;
               const uint32_t dst = base_s + OFF_Q + x * TILE;
               mbar_arrive_expect_tx(bar(BAR_QF + x), (uint32_t)TILE);
-              tma_load_3d(dst, &tq, 0, c.hq, row, bar(BAR_QF + x));
-              tma_load_3d(dst + HALF, &tq, 64, c.hq, row, bar(BAR_QF + x));
+              tma_load_3d(dst, &tq, 0, head, row, bar(BAR_QF + x));
+              tma_load_3d(dst + HALF, &tq, 64, head, row, bar(BAR_QF + x));
             } else {
               mbar_arrive(bar(BAR_QF + x));
             }
@@ -798,9 +841,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       if (split) {
         if (c.ustart <= lo) c.end = true;         // this unit opens the range: done
-        else prev_unit(a, c);
+        else prev_unit(a, c, hp);
       } else {
-        skip_units(a, c, (sg & 1) ? 2 * cta + 1 : 2 * P - 1 - 2 * cta);
+        skip_units(a, c, (sg & 1) ? 2 * cta + 1 : 2 * P - 1 - 2 * cta, hp);
       }
     }
   } else if (warp == WARP_MMA) {
@@ -929,7 +972,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const int j0 = d->j0;
       const int jend = min(d->j1, x == 0 ? d->nblk_a : d->nblk_b);
-      const int pos_min = d->pmin_a + x * BM;
+      const int pos_min = HP ? (x == 0 ? d->pmin_a : d->pmin_b) : d->pmin_a + x * BM;
       const int pos_r = min(pos_min + r, d->L - 1);   // padding rows clamp to the last key
 
       // Running max (scaled, log2 domain) and sum.  The max starts finite and
@@ -1010,8 +1053,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         par ^= PAR_O;
         tc_fence_after();
       }
-      const int qrow0 = d->qrow0 + x * BM;        // q row of this tile's row 0
-      const int hq = d->hq;
+      // q row of this tile's row 0, and its head
+      const int qrow0 = HP ? (x == 0 ? d->qrow0 : d->qrow_b) : d->qrow0 + x * BM;
+      const int hq = HP ? (x == 0 ? d->hq : d->hq_b) : d->hq;
       const int nown = d->nown;
       const bool row_valid = r < (x == 0 ? d->rows_a : d->rows_b);
       const float inv = 1.0f / l_run;
@@ -1281,9 +1325,11 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
+    for (auto fn : {prefill_kernel<false>, prefill_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+    }
     configured = true;
   }
   if (a.ctas <= 0 || a.ctas > kMaxPrefillCtas || !a.workspace) return cudaErrorInvalidValue;
@@ -1291,7 +1337,16 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
   PrefillParams prm{a, reinterpret_cast<uint32_t*>(ws),
                     reinterpret_cast<float*>(ws + ws_counter_bytes(a.ctas)),
                     reinterpret_cast<float4*>(ws + ws_counter_bytes(a.ctas) + ws_lse_bytes(a.ctas))};
-  prefill_kernel<<<a.ctas, NUM_THREADS, SMEM_BYTES, s>>>(tk, tv, tq, prm);
+  // The head-pair build (units of two heads on one row tile) only where a
+  // chunk ends in a single row tile: max_q_len tells it exactly for one
+  // sequence and is a proxy for a batch; either build is correct for any
+  // launch, the other one is a little faster where no unit pairs heads.
+  const bool hp = (a.num_q_heads / a.num_kv_heads) % 2 == 0 && a.max_q_len % (2 * BM) != 0 &&
+                  a.max_q_len % (2 * BM) <= BM;
+  if (hp)
+    prefill_kernel<true><<<a.ctas, NUM_THREADS, SMEM_BYTES, s>>>(tk, tv, tq, prm);
+  else
+    prefill_kernel<false><<<a.ctas, NUM_THREADS, SMEM_BYTES, s>>>(tk, tv, tq, prm);
   return cudaGetLastError();
 }
 
