@@ -40,12 +40,12 @@ from paged_kv_flash_gb300 import workloads as W  # noqa: E402
 
 # DRAM bytes (read + write) per prefill launch of the mixed step, from one ncu
 # capture of `bench.py --profile-case prefill_chunk` (2,048 rows against
-# 16,384 positions: 142.3 MB, profiles/prefill_kernel_chunk2048_ctx16384.md),
+# 16,384 positions: 142.5 MB, profiles/prefill_kernel_chunk2048_ctx16384.md),
 # scaled to the mixed step's average context per launch (15,235 positions):
 # K/V traffic grows with the context a chunk attends to.  Re-measure (or set
 # to None) whenever the prefill kernel changes.
-PREFILL_TRAFFIC_BYTES = 132.3e6
-PREFILL_TRAFFIC_NOTE = ("ncu dram read+write of a 2,048 x 16,384 launch (142.3 MB) scaled by "
+PREFILL_TRAFFIC_BYTES = 132.5e6
+PREFILL_TRAFFIC_NOTE = ("ncu dram read+write of a 2,048 x 16,384 launch (142.5 MB) scaled by "
                         "mean context 15,235 / 16,384")
 
 METRIC = ("decode attn µs & HBM GB/s (% of 8 TB/s); prefill attn TFLOP/s (% of peak)")
