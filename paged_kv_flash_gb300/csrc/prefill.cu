@@ -30,11 +30,14 @@
 // but 0 * NaN is NaN).
 //
 // Work split: see "Work decomposition" below.  A unit of work cut between
-// CTAs is finished by whichever of its CTAs completes its part last: each
-// part is written (normalised O, log2-domain lse) to the caller's workspace,
-// a per-unit counter in the workspace counts the parts, and the last one
-// merges them with the log-sum-exp rule ("Split-KV decoding") and resets the
-// counter to zero for the next call.
+// CTAs is finished by the CTA holding its last blocks: every other part is
+// written (normalised O, log2-domain lse) to the caller's workspace and
+// counted in a per-unit counter there; that CTA waits (bounded) for the
+// count, merges the parts with its own by the log-sum-exp rule ("Split-KV
+// decoding") and resets the counter to zero for the next call.  The kernel
+// has two builds: with the template flag HP, a unit whose second row tile
+// is past the chunk may hold the same rows of two query heads instead; the
+// host picks the build per launch.
 //
 // Every wait is bounded (wall clock, one second); a wait that runs out sets
 // the device error word and an abort flag that makes every role leave its
