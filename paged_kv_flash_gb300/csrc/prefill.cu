@@ -636,10 +636,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the first block's page ids of the first sequence: usually needed first
     if (lane < BN / kPageSize && lane < a.max_pages)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + lane));
-    // whole units' makespan vs the split share (both times units * P)
+    // whole units' makespan vs the split share (in double: the products of
+    // large launches would not fit 64 bits, and this is only an estimate)
     auto cut = [&](long long w, int um, long long n) {
-      const long long per = (n + P - 1) / P;
-      return n > 0 && max((long long)um * n * P, per * w * P) > (w + (long long)kSplitGain * P) * n;
+      if (n <= 0) return false;
+      const double per = (double)((n + P - 1) / P);
+      const double whole = fmax((double)um, per * (double)w / (double)n);
+      return whole > (double)w / (double)P + (double)kSplitGain;
     };
     int umax = 0;
     long long units = 0;
