@@ -237,12 +237,16 @@ pkv_status pkv_prefill_plan(int32_t* ctas, size_t* workspace_bytes, size_t* zero
  *            bytes (part counters) must be zero before its first use; every
  *            call that completes leaves them zero again, so a workspace is
  *            zeroed once and reused (zero it again after PKV_ERR_TIMEOUT).
- *            The call runs one persistent CTA per SM over an even share of
- *            all (sequence, query-tile pair, head, key block) work; a unit of
- *            work cut between CTAs leaves its parts there, and the CTA that
- *            finishes the last part merges them (the log-sum-exp rule of
- *            "Split-KV decoding").  PKV_ERR_INVALID if NULL, unaligned or
- *            too small.  Calls that share a workspace must not overlap.
+ *            The call runs one persistent CTA per SM.  Each launch either
+ *            cuts all (sequence, query-tile pair, head, key block) work into
+ *            even shares or gives the CTAs whole units, whichever its
+ *            estimate finishes sooner; where a chunk ends in a single
+ *            128-row tile and the query heads of a KV head come in pairs, a
+ *            unit may hold that tile for two heads.  A unit cut between CTAs
+ *            leaves its other parts in the workspace, and the CTA holding its
+ *            last blocks merges them (the log-sum-exp rule of "Split-KV
+ *            decoding").  PKV_ERR_INVALID if NULL, unaligned or too small.
+ *            Calls that share a workspace must not overlap.
  *  out       bf16 [total_q][num_q_heads][128]; lse fp32 [total_q][num_q_heads]
  *            or NULL.
  * bf16 pools only (PKV_ERR_UNSUPPORTED for INT8).
