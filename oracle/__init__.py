@@ -58,6 +58,8 @@ def _load():
         lib.orc_qkv_norm_rope_append.restype = I
         lib.orc_bf16_from_double.argtypes = [ctypes.c_double]
         lib.orc_bf16_from_double.restype = ctypes.c_uint16
+        lib.orc_rsqrt_rn.argtypes = [ctypes.c_float]
+        lib.orc_rsqrt_rn.restype = ctypes.c_float
         _lib = lib
     return _lib
 
@@ -192,3 +194,10 @@ def qkv_norm_rope_append(qkv, Hq, Hkv, q_w, k_w, eps, cos_tab, sin_tab, cu_new, 
     if rc != 0:
         raise ValueError("oracle: position outside the block table or the RoPE table")
     return q_out, k_pool, v_pool
+
+
+def rsqrt_rn(z: float) -> np.float32:
+    """The float nearest to 1 / sqrt(z) (ties to even) for a positive normal
+    float z: the RMSNorm's reciprocal square root in the fused attention
+    inputs."""
+    return np.float32(_load().orc_rsqrt_rn(float(np.float32(z))))

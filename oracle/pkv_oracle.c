@@ -416,10 +416,16 @@ int orc_kv_append_int8(int8_t* pool_k, int8_t* pool_v, float* k_scale, float* v_
  * 2 RoPE, 1 write).  The pages give no formulas; readings (stated once here
  * and in the build's notes), with the chain taken to be fp32 GPU kernels
  * that store bf16:
- *  - RMSNorm over one head's D channels: r = 1 / sqrt(mean_c x_c^2 + eps)
- *    (mean in fp64, exact for bf16 inputs of ordinary range; r rounded to
- *    fp32), n_c = bf16((x_c * r) * w_c) with both products in fp32.  A NULL
- *    weight means that part has no norm (n = x).
+ *  - RMSNorm over one head's D channels, the chain's fp32 norm kernel:
+ *    ms = fp32(sum_c x_c^2 / D) (the exact sum, rounded once; D a power of
+ *    two), z = fp32(ms + eps) with eps an fp32 value, r = fp32(1 / sqrt(z))
+ *    correctly rounded (orc_rsqrt_rn), n_c = bf16((x_c * r) * w_c) with
+ *    both products in fp32.  Every step is one IEEE fp32 rounding of an
+ *    exactly defined value, so the result does not depend on the order in
+ *    which a kernel sums the squares.  The sum is exact in fp64 while the
+ *    head's values span at most 2^15 in magnitude (53 bits hold the 16-bit
+ *    squares and 7 bits of carries).  A NULL weight means that part has no
+ *    norm (n = x).
  *  - RoPE by halves (channel i pairs with i + D/2, i < D/2) at the token's
  *    position p, with cos/sin from a caller table [max_pos][D/2], every
  *    product and sum in fp32: o_i = bf16(n_i cos - n_{i+D/2} sin),
@@ -453,8 +459,54 @@ static uint16_t bf16_bits_from_double(double v) {
   return sign | (uint16_t)(u >> 16);
 }
 
+/* Sign of m^2 z - 1 for m = M 2^a (M an integer below 2^26) and z a positive
+ * normal float, in exact integer arithmetic. */
+static int sq_times_z_vs_one(uint64_t M, int a, float z) {
+  int bz;
+  const double fz = frexp((double)z, &bz);              /* z = fz 2^bz, fz in [1/2, 1) */
+  const uint64_t Z = (uint64_t)ldexp(fz, 24);           /* z = Z 2^(bz - 24), exact */
+  const int e = 2 * a + bz - 24;                        /* m^2 z = M^2 Z 2^e */
+  const unsigned __int128 P = (unsigned __int128)(M * M) * Z;   /* below 2^76 */
+  if (P == 0) return -1;
+  if (e >= 0) return (e == 0 && P == 1) ? 0 : 1;
+  if (-e >= 127) return -1;
+  const unsigned __int128 one = (unsigned __int128)1 << -e;
+  return P < one ? -1 : (P > one ? 1 : 0);
+}
+
+/* The float nearest to 1 / sqrt(z), ties to even, for a positive normal
+ * float z.  Start from the double-precision quotient (within one float step
+ * of the answer) and test, exactly, where 1/sqrt(z) lies against the
+ * midpoints between the candidate and its neighbours: y > m iff m^2 z < 1. */
+float orc_rsqrt_rn(float z) {
+  float r = (float)(1.0 / sqrt((double)z));
+  for (int it = 0; it < 4; ++it) {
+    int er;
+    const double fr = frexp((double)r, &er);            /* r = fr 2^er */
+    const uint64_t R = (uint64_t)ldexp(fr, 24);         /* r = R 2^(er - 24), R in [2^23, 2^24) */
+    const int pow2 = R == (1ull << 23);                 /* the step below r halves */
+    /* upper midpoint (R + 1/2) 2^(er - 24); lower (R - 1/2) 2^(er - 24), or
+     * (R - 1/4) 2^(er - 24) when r is a power of two */
+    const int hi = sq_times_z_vs_one(2 * R + 1, er - 25, z);
+    const int lo = pow2 ? sq_times_z_vs_one(4 * R - 1, er - 26, z)
+                        : sq_times_z_vs_one(2 * R - 1, er - 25, z);
+    if (hi < 0) {                     /* 1/sqrt(z) above the upper midpoint */
+      r = nextafterf(r, INFINITY);
+      continue;
+    }
+    if (lo > 0) {                     /* 1/sqrt(z) below the lower midpoint */
+      r = nextafterf(r, 0.0f);
+      continue;
+    }
+    if (hi == 0) return (R & 1) ? nextafterf(r, INFINITY) : r;   /* a tie: the even one */
+    if (lo == 0) return (R & 1) ? nextafterf(r, 0.0f) : r;
+    return r;
+  }
+  return r;
+}
+
 /* RMSNorm (if w) then RoPE (if cos_row) of one head vector of D bf16 values. */
-static void norm_rope(const uint16_t* x, int D, const float* w, double eps, const float* cos_row,
+static void norm_rope(const uint16_t* x, int D, const float* w, float eps, const float* cos_row,
                       const float* sin_row, uint16_t* out) {
   uint16_t n[1024];
   if (w) {
@@ -463,7 +515,9 @@ static void norm_rope(const uint16_t* x, int D, const float* w, double eps, cons
       const double v = bf16_bits_to_double(x[c]);
       ss += v * v;
     }
-    const float r = (float)(1.0 / sqrt(ss / D + eps));
+    const float ms = (float)(ss / D);
+    const float z = ms + eps;
+    const float r = orc_rsqrt_rn(z);
     for (int c = 0; c < D; ++c) {
       const float xr = bf16_bits_to_float(x[c]) * r;
       const float y = xr * w[c];
@@ -509,10 +563,10 @@ int orc_qkv_norm_rope_append(const uint16_t* qkv, int Hq, int Hkv, int D, const 
       const float* sr = sin_tab ? sin_tab + (size_t)p * (D / 2) : NULL;
       const uint16_t* row = qkv + (size_t)t * H * D;
       for (int h = 0; h < Hq; ++h)
-        norm_rope(row + (size_t)h * D, D, q_w, eps, cr, sr, q_out + ((size_t)t * Hq + h) * D);
+        norm_rope(row + (size_t)h * D, D, q_w, (float)eps, cr, sr, q_out + ((size_t)t * Hq + h) * D);
       for (int h = 0; h < Hkv; ++h) {
         const size_t dst = ((size_t)(page * Hkv + h) * page_size + slot) * D;
-        norm_rope(row + (size_t)(Hq + h) * D, D, k_w, eps, cr, sr, pool_k + dst);
+        norm_rope(row + (size_t)(Hq + h) * D, D, k_w, (float)eps, cr, sr, pool_k + dst);
         memcpy(pool_v + dst, row + (size_t)(Hq + Hkv + h) * D, sizeof(uint16_t) * (size_t)D);
       }
     }

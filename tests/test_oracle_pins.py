@@ -550,3 +550,60 @@ def test_q_and_k_take_their_own_weights():
     qf = W.bits_to_float(q[0, 0])
     kf = W.bits_to_float(k[bt[0, 0], 0, 0])
     assert np.array_equal(kf, qf * np.float32(0.5))      # halving is exact in bf16
+
+
+def _nearest_float_to_rsqrt(z):
+    """Brute force in exact rational arithmetic: among the floats around
+    1/sqrt(z), the one whose rounding interval (the midpoints with its two
+    neighbours) holds 1/sqrt(z); y lies above a midpoint m iff m^2 z < 1."""
+    from fractions import Fraction
+    zq = Fraction(float(z))
+    r = np.float32(1.0 / np.sqrt(np.float64(z)))
+    down, up = np.float32(0), np.float32(np.inf)
+    cands = [np.nextafter(np.nextafter(r, down), down), np.nextafter(r, down), r,
+             np.nextafter(r, up), np.nextafter(np.nextafter(r, up), up)]
+    for c in cands:
+        cq = Fraction(float(c))
+        lo = (Fraction(float(np.nextafter(c, down))) + cq) / 2
+        hi = (Fraction(float(np.nextafter(c, up))) + cq) / 2
+        if lo * lo * zq <= 1 <= hi * hi * zq:
+            return np.float32(c)
+    raise AssertionError(f"no candidate for z = {float(z)}")
+
+
+def test_rsqrt_rn_is_the_nearest_float():
+    """The RMSNorm's reciprocal square root (fused attention inputs, TileInfer.jl
+    "Performance" page, "Fused kernels, FlashAttention and PagedAttention":
+    the chain's fp32 norm) is the correctly rounded 1/sqrt(z): checked in
+    exact rational arithmetic on seeded floats spread over the normal range,
+    on both sides of powers of two, and on powers of four (exact results)."""
+    rng = np.random.default_rng(5)
+    zs = list((rng.uniform(0.5, 1.0, 300) * np.exp2(rng.integers(-120, 120, 300)))
+              .astype(np.float32))
+    for e in range(-60, 61, 7):
+        p = np.float32(2.0 ** e)
+        zs += [p, np.nextafter(p, np.float32(0)), np.nextafter(p, np.float32(np.inf))]
+    zs += [np.float32(x) for x in (1.0, 6.25, 3.0, 1e-6, 1.0 + 1e-6)]
+    for z in zs:
+        got, want = oracle.rsqrt_rn(z), _nearest_float_to_rsqrt(z)
+        assert got == want, (float(z), float(got), float(want))
+    for k in range(-30, 31):
+        assert oracle.rsqrt_rn(np.float32(4.0 ** k)) == np.float32(2.0 ** -k)
+
+
+def test_norm_mean_square_rounds_once_from_the_exact_sum():
+    """The RMSNorm's mean square is the exact sum of squares rounded once to
+    fp32.  x = (2, 2^-11, 2^-23, 0), D = 4: the squares sum to 4 + 2^-22 +
+    2^-46, so the mean 1 + 2^-24 + 2^-48 lies just above the midpoint of 1
+    and 1 + 2^-23 and rounds up; r = 1/sqrt(1 + 2^-23) rounds to 1 - 2^-24.
+    (A running fp32 sum ties 4 + 2^-22 to 4 and gives r = 1.)  The weight
+    w0 = 1 + 3 * 2^-8 puts 2 r w0 next to the bf16 tie 2 + 3 * 2^-7: with
+    r = 1 - 2^-24 the fp32 product 2 + 3 * 2^-7 - 2^-22 rounds down to
+    2.015625 (r = 1 would tie to even, 2.03125)."""
+    D = 4
+    x = np.array([2.0, 2.0 ** -11, 2.0 ** -23, 0.0], np.float32)
+    w = np.array([1.0 + 3 * 2.0 ** -8, 1.0, 1.0, 1.0], np.float32)
+    assert oracle.rsqrt_rn(np.float32(1.0 + 2.0 ** -23)) == np.float32(1.0 - 2.0 ** -24)
+    qkv, kp, vp, cu, bt, sl = _one_token_case(D, _bits(x))
+    q, _, _ = oracle.qkv_norm_rope_append(qkv, 1, 1, w, w, 0.0, None, None, cu, bt, sl, kp, vp)
+    assert W.bits_to_float(q[0, 0])[0] == np.float32(2.015625)
