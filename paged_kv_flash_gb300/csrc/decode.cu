@@ -707,6 +707,7 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
 #pragma unroll
     for (int j = 0; j < 4; ++j) o[mt][j] = 0.f;
   float m_used = -INFINITY, l = 0.f, cs = 0.f;
+  float pc = 0.f;                     // power-of-two multiplier of P' (head row r)
 
   bool failed = false;
   int i_fail = 0;
@@ -770,18 +771,6 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
       alpha = fast_exp2(m_used - pm);
       m_used = pm;
       l *= alpha;
-      cs *= alpha;
-    }
-    if (__any_sync(FULL, grow)) {
-      const float a0 = __shfl_sync(FULL, alpha, 8 * qd);       // head 2qd's row
-      const float a1 = __shfl_sync(FULL, alpha, 8 * qd + 4);   // head 2qd + 1's row
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= a0;
-        o[mt][1] *= a1;
-        o[mt][2] *= a0;
-        o[mt][3] *= a1;
-      }
     }
     float pv[2][2];
 #pragma unroll
@@ -793,8 +782,38 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
         // masked keys: p = 0, and their (unwritten) scale must not reach the MMA
         pv[t][e] = (8 * t + 2 * qd + e < nvalid) ? p * (e ? vsc[t].y : vsc[t].x) : 0.f;
       }
-    const uint32_t pb0 = pack_f16x2(pv[0][0], pv[0][1]);
-    const uint32_t pb1 = pack_f16x2(pv[1][0], pv[1][1]);
+    // P' = p * v_scale goes to the MMA in f16, whose range (2^-24 .. 65504)
+    // is far narrower than the V scales' (amax / 127 of any bf16 vector).  The
+    // head carries a power-of-two multiplier pc (0 until a nonzero P' is
+    // seen): it is lowered so that the page's largest P' * pc stays below
+    // 2^14 and set, when first needed, so that it lands in [2^13, 2^14).  O
+    // and the bias sum hold P' * pc units, rescaled exactly when pc moves, and
+    // the epilogue divides pc out.  Scaling every V by 2^k scales pc by 2^-k
+    // and leaves the f16 values unchanged.
+    float pvm = fmaxf(fmaxf(pv[0][0], pv[0][1]), fmaxf(pv[1][0], pv[1][1]));
+    pvm = fmaxf(pvm, __shfl_xor_sync(FULL, pvm, 1));
+    pvm = fmaxf(pvm, __shfl_xor_sync(FULL, pvm, 2));
+    const int pve = __float_as_int(pvm) >> 23;               // biased exponent (pvm >= 0)
+    const float pc_want = __int_as_float(min(254, 267 - pve) << 23);   // 2^(13 - floor(log2 pvm))
+    float f = alpha;
+    if (pve > 0 && (pc == 0.f || pc_want < pc)) {             // unset, or P' * pc >= 2^14
+      if (pc != 0.f) f *= pc_want / pc;                       // exact: powers of two
+      pc = pc_want;
+    }
+    cs *= f;
+    if (__any_sync(FULL, f != 1.f)) {
+      const float a0 = __shfl_sync(FULL, f, 8 * qd);           // head 2qd's row
+      const float a1 = __shfl_sync(FULL, f, 8 * qd + 4);       // head 2qd + 1's row
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= a0;
+        o[mt][1] *= a1;
+        o[mt][2] *= a0;
+        o[mt][3] *= a1;
+      }
+    }
+    const uint32_t pb0 = pack_f16x2(pv[0][0] * pc, pv[0][1] * pc);
+    const uint32_t pb1 = pack_f16x2(pv[1][0] * pc, pv[1][1] * pc);
     {
       const float2 f0 = unpack_f16x2(pb0), f1 = unpack_f16x2(pb1);
       cs += (f0.x + f0.y) + (f1.x + f1.y);
@@ -837,6 +856,10 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
   cs += __shfl_xor_sync(FULL, cs, 2);
   const float bA = kBias * __shfl_sync(FULL, cs, 8 * qd);
   const float bB = kBias * __shfl_sync(FULL, cs, 8 * qd + 4);
+  // O and the bias sum are in units of pc: divide it out (pc = 0: no P' was
+  // nonzero, O is 0)
+  const float ipc = pc != 0.f ? 1.f / pc : 1.f;
+  const float iA = __shfl_sync(FULL, ipc, 8 * qd), iB = __shfl_sync(FULL, ipc, 8 * qd + 4);
   float* wo = reinterpret_cast<float*>(wbuf);              // [G][128]
   float* wm = wo + G * kHeadDim;                           // [G]
   float* wl = wm + G;                                      // [G]
@@ -846,10 +869,12 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
     const int ch = 16 * r + 4 * (mt >> 1) + 2 * (mt & 1);
     if (c0 < G)
       *reinterpret_cast<float2*>(wo + c0 * kHeadDim + ch) =
-          failed ? make_float2(0.f, 0.f) : make_float2(o[mt][0] - bA, o[mt][2] - bA);
+          failed ? make_float2(0.f, 0.f)
+                 : make_float2((o[mt][0] - bA) * iA, (o[mt][2] - bA) * iA);
     if (c1 < G)
       *reinterpret_cast<float2*>(wo + c1 * kHeadDim + ch) =
-          failed ? make_float2(0.f, 0.f) : make_float2(o[mt][1] - bB, o[mt][3] - bB);
+          failed ? make_float2(0.f, 0.f)
+                 : make_float2((o[mt][1] - bB) * iB, (o[mt][3] - bB) * iB);
   }
   if (qd == 0 && r < G) {
     wm[r] = failed ? -INFINITY : m_used;

@@ -249,3 +249,53 @@ def test_int8_empty_context_and_single_keys(pk):
         out, lse = gpu_decode(pk, case, splits, int8_pools=pools, smooth=w)
         check_out(out, ro, f"int8 edge splits={splits}")
         check_lse(lse, rl, f"int8 edge splits={splits}")
+
+
+def scaled_bits(bits: np.ndarray, k: int) -> np.ndarray:
+    """bf16 bit patterns of the values times 2^k (exact for these ranges:
+    neither subnormal nor overflowing in bf16)."""
+    x = W.bits_to_float(bits).astype(np.float64) * 2.0 ** k
+    out = W.to_bf16_bits(x.astype(np.float32))
+    assert np.array_equal(W.bits_to_float(out).astype(np.float64), x)
+    return out
+
+
+@pytest.mark.parametrize("k", [-16, 8])
+def test_int8_decode_is_exact_under_power_of_two_v_scaling(pk, k):
+    """V times 2^k gives the same INT8 codes and scales exactly 2^k times the
+    originals (scale = max|v| / 127 and the quotient v / scale are exact
+    under a power-of-two factor), so exact attention over the cache is 2^k
+    times the unscaled one and the lse is unchanged ("INT8 KV cache" of the
+    TileInfer.jl "Performance" page; the softmax weights do not depend on
+    V).  The GPU output must follow at any V magnitude: at 2^-16 the
+    products p * v_scale lie far below the smallest normal f16, at 2^8 far
+    above the unit range.  The 32,768-position cache of the INT8 workload,
+    batch 1, at the heuristic's split count and at 1 and 9 splits; the
+    scaled output equals 2^k times the unscaled GPU output to a relative
+    1e-2 per element, and matches the fp64 oracle within the decode
+    tolerance once 2^k is divided out."""
+    app, q = W.int8_long_decode(B=1)
+    w = app.k_smooth
+    outs = {}
+    for kk in (0, k):
+        v_new = app.v_new if kk == 0 else scaled_bits(app.v_new, kk)
+        pool = pk.Pool.empty(app.layout.num_pages, app.Hkv, dtype=torch.int8)
+        pk.kv_append(pool, dev_bf16(app.k_new), dev_bf16(v_new), dev(app.cu_new),
+                     dev(app.layout.block_table), dev(app.seq_lens), k_smooth=dev(w))
+        assert pk.poll_device_error() == pk.OK
+        pools = tuple(t.cpu().numpy() for t in (pool.k, pool.v, pool.k_scale, pool.v_scale))
+        case = W.DecodeCase(32, app.Hkv, app.seq_lens, app.layout, q, None, None)
+        ro, rl = oracle_decode(case, int8_pools=pools, smooth=w)
+        for splits in (0, 1, 9):
+            out, lse = gpu_decode(pk, case, splits, int8_pools=pools, smooth=w)
+            o = out.float().cpu().numpy().astype(np.float64) * 2.0 ** -kk
+            check_out(torch.from_numpy(o), ro * 2.0 ** -kk,
+                      f"int8 V x 2^{kk} splits={splits}, 2^{kk} divided out")
+            check_lse(lse, rl, f"int8 V x 2^{kk} splits={splits}")
+            outs[(kk, splits)] = (o, lse.cpu().numpy())
+    for splits in (0, 1, 9):
+        o0, l0 = outs[(0, splits)]
+        ok, lk = outs[(k, splits)]
+        rel = np.abs(ok - o0) / np.maximum(np.abs(o0), 1e-30)
+        assert (rel <= 1e-2).all(), (k, splits, float(rel.max()))
+        assert np.array_equal(l0, lk), (k, splits)
