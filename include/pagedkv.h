@@ -314,9 +314,11 @@ pkv_status pkv_paged_attn_decode_multi(const pkv_pool* pool, const void* q, int3
  *  qkv        bf16 [num_tokens][num_q_heads + 2 Hkv][128]: q heads, then k
  *             heads, then v heads (16-byte aligned).
  *  q_norm_w,  fp32 [128] RMSNorm weights of q and of k, or NULL for no norm
- *  k_norm_w   on that part; eps > 0 typical (1e-6).  n_c = bf16(x_c * r *
- *             w_c), r = 1 / sqrt(mean_c x_c^2 + eps), fp32 (r correctly
- *             rounded).
+ *  k_norm_w   on that part; eps > 0 typical (1e-6).  n_c = bf16((x_c * r)
+ *             * w_c) with fp32 products, r = 1 / sqrt(z) correctly rounded,
+ *             z = fp32(ms + eps), ms = the exact mean of x_c^2 rounded once
+ *             to fp32 (exact while a head vector's values span at most 2^20
+ *             in magnitude), so no summation order enters the result.
  *  rope_cos,  fp32 [max_pos][64] each, or both NULL for no RoPE.  Channel i
  *  rope_sin   pairs with i + 64 at the token's position p: o_i = bf16(n_i
  *             cos[p][i] - n_{i+64} sin[p][i]), o_{i+64} = bf16(n_{i+64}

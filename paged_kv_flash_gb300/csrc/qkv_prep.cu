@@ -5,8 +5,9 @@
 // that replaces 3 copies, 2 norms, 2 RoPE and 1 write).
 //
 // Steps per head vector x (128 bf16 channels), as the unfused chain would
-// run them: RMSNorm n_c = bf16(x_c * r * w_c), r = 1/sqrt(mean x^2 + eps)
-// (fp32; r correctly rounded); RoPE by halves with the caller's cos/sin
+// run them: RMSNorm n_c = bf16(x_c * r * w_c), r = 1/sqrt(z) correctly
+// rounded, z = fp32(ms + eps), ms = the exact mean of x^2 rounded once to
+// fp32 (each step one fp32 rounding, so no summation order enters); RoPE by halves with the caller's cos/sin
 // table at the token's position, o_i = bf16(n_i cos - n_{i+64} sin),
 // o_{i+64} = bf16(n_{i+64} cos + n_i sin) (fp32, each product and sum
 // rounded once); V copied.  A NULL weight skips that norm, a NULL table
@@ -47,6 +48,48 @@ struct Rope {
   float2 c[4], s[4];  // cos/sin of this lane's channel pairs at the token's position
 };
 
+// The mean of the squares of one head vector's 128 bf16 values, rounded once
+// to fp32 from the exact sum, so that the result does not depend on the
+// order of summation.  Each lane holds 16 of the values (words wa, wb); the
+// 8 lanes of the head reduce by shuffles.  A bf16 magnitude is m 2^(E - 134)
+// with an 8-bit integer m (E the biased exponent, 1 for subnormals), so its
+// square is m^2 2^(2E - 268) with m^2 < 2^16.  The squares are added as
+// integers in units of 2^(2 Emax - 308), Emax the head's largest exponent:
+// m^2 << (2 (E - Emax) + 40), at most 2^56 each, 2^63 for all 128.  Exact
+// while the values span at most 2^20 in magnitude (smaller squares are
+// dropped below 2^-40 of the largest); the one rounding is the conversion
+// of the 64-bit sum to fp32.  Caller contract: finite inputs.
+__device__ __forceinline__ float mean_square_rn(const uint32_t (&wa)[4],
+                                                const uint32_t (&wb)[4]) {
+  uint32_t mx = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) mx = __vmaxu2(__vmaxu2(mx, wa[e] & 0x7fff7fffu), wb[e] & 0x7fff7fffu);
+  mx = max(mx & 0xffffu, mx >> 16);
+#pragma unroll
+  for (int o = 4; o >= 1; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const int emax = max(1, (int)(mx >> 7));
+  unsigned long long acc = 0;
+  const auto add = [&](uint32_t h) {
+    h &= 0x7fffu;
+    const int E = (int)(h >> 7);
+    const uint32_t m = (h & 0x7fu) | (E ? 0x80u : 0u);
+    const int sh = 2 * (max(E, 1) - emax) + 40;
+    if (sh >= 0) acc += (unsigned long long)(m * m) << sh;
+  };
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    add(wa[e]);
+    add(wa[e] >> 16);
+    add(wb[e]);
+    add(wb[e] >> 16);
+  }
+#pragma unroll
+  for (int o = 4; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  // sum / 128 = acc 2^(2 emax - 315): scaling by a power of two is exact
+  // while the result is a normal float
+  return ldexpf(__ull2float_rn(acc), 2 * emax - 315);
+}
+
 // Norm, rotate (or copy) head h of token t and store it.  Every lane of the
 // warp calls this together (the sum of squares is reduced with shuffles);
 // lanes of a head past H compute on zeros and store nothing.
@@ -62,14 +105,7 @@ __device__ __forceinline__ void finish_head(const pkv_host::QkvPrepLaunch& a, in
     A[e] = unpack2(wa[e]);
     B[e] = unpack2(wb[e]);
   }
-  float2 acc = mul2(A[0], A[0]);
-#pragma unroll
-  for (int e = 1; e < 4; ++e) acc = fma2(A[e], A[e], acc);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) acc = fma2(B[e], B[e], acc);
-  float ss = __fadd_rn(acc.x, acc.y);
-#pragma unroll
-  for (int o = 4; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+  const float ms = mean_square_rn(wa, wb);
 
   const float* w = kind == 0 ? a.q_w : kind == 1 ? a.k_w : nullptr;
   uint32_t oa[4], ob[4];
@@ -79,8 +115,9 @@ __device__ __forceinline__ void finish_head(const pkv_host::QkvPrepLaunch& a, in
     ob[e] = wb[e];
   }
   if (w) {
-    // r correctly rounded; the chain's norm kernel stores bf16
-    const float r = __frsqrt_rn(__fadd_rn(__fmul_rn(ss, 1.0f / kHeadDim), a.eps));
+    // the chain's fp32 norm: z = fp32(mean + eps), r = 1/sqrt(z) correctly
+    // rounded; it stores bf16
+    const float r = __frsqrt_rn(__fadd_rn(ms, a.eps));
     const float2 rr = make_float2(r, r);
     const float4* w4 = reinterpret_cast<const float4*>(w) + 2 * l8;
     const float4 w0 = __ldg(w4), w1 = __ldg(w4 + 1), w2 = __ldg(w4 + 16), w3 = __ldg(w4 + 17);
