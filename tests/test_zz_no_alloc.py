@@ -6,7 +6,8 @@ owns all device memory and forbids cudaMalloc on its threads, or code that
 cannot afford an allocation's implicit synchronisation.  For them the
 library keeps the split partials in a fixed 16 MiB device array of its own.
 These tests call that entry point through the C ABI and compare it with the
-workspace entry point, on consecutive calls that share the array.
+workspace entry point, on consecutive calls that share the array, and with
+the fp64 oracle.
 
 The file name sorts last so that a run that stops at the first failure has
 already run every other test.
@@ -16,6 +17,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 from paged_kv_flash_gb300 import workloads as W
 from tests.helpers import check_lse, check_out, dev, dev_bf16, host_f32
 
@@ -84,3 +86,14 @@ def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
         assert pk.poll_device_error() == pk.OK
         check_out(out, host_f32(ref_out).astype(np.float64), "noalloc vs workspace decode")
         check_lse(lse, ref_lse.cpu().numpy().astype(np.float64), "noalloc vs workspace decode")
+        # and against the fp64 oracle: every row of the single sequence, a
+        # seeded sample of 16 of the 64 sequences (the lowered-split call)
+        rows = np.arange(case.B, dtype=np.int32) if case.B <= 16 else np.sort(
+            np.random.default_rng(70).choice(case.B, 16, replace=False)).astype(np.int32)
+        ro, rl = oracle.paged_attention(case.k_pool, case.v_pool, case.q,
+                                        np.arange(case.B + 1, dtype=np.int32),
+                                        case.layout.block_table, case.seq_lens, case.scale,
+                                        rows=rows)
+        idx = torch.from_numpy(rows).long().cuda()
+        check_out(out[idx], ro, "noalloc vs oracle")
+        check_lse(lse[idx], rl, "noalloc vs oracle")
