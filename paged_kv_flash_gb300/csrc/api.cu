@@ -2,26 +2,52 @@
 // include/pagedkv.h): host-side argument checks, the split-count heuristic
 // and kernel dispatch.  Nothing here allocates device or host memory.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace pkv_host {
 
+namespace {
+constexpr int kMaxDevices = 64;
+}
+
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  static int cached_dev = -1, cached = 0;
-  if (dev != cached_dev) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 152;
-    cached = n;
-    cached_dev = dev;
-  }
-  return cached;
+  static std::atomic<int> cached[kMaxDevices];     // 0: not looked up yet
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  int n = slot ? cached[dev].load(std::memory_order_relaxed) : 0;
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 152;
+  if (slot) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  // (kernel, device) pairs already raised; a fixed table, no allocation
+  // (when it is full the attribute is simply set on every launch)
+  struct Entry {
+    const void* kernel;
+    int dev;
+  };
+  static std::mutex mu;
+  static Entry done[512];
+  static int n_done = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_done; ++i)
+    if (done[i].kernel == kernel && done[i].dev == dev) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && n_done < 512) done[n_done++] = {kernel, dev};
+  return e;
 }
 
 }  // namespace pkv_host

@@ -240,4 +240,9 @@ inline uint32_t take_error_word(const void* symbol, cudaStream_t s) {
   return h;
 }
 int sm_count();                 // cached SM count of the current device
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per (kernel,
+// current device): the attribute belongs to the device's context, so a
+// process flag would skip a second device.  Thread-safe.
+cudaError_t set_max_dynamic_smem(const void* kernel, int bytes);
 }

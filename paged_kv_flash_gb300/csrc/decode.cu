@@ -908,13 +908,9 @@ template <int G, bool FUSED>
 cudaError_t launch_split_as(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
   using C = Cfg<G>;
   constexpr int smem = 1024 + pkv_host::kDecodeWarps * C::NBUF * C::BUF;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, FUSED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = pkv_host::set_max_dynamic_smem(
+      reinterpret_cast<const void*>(decode_split_kernel<G, FUSED>), smem);
+  if (e != cudaSuccess) return e;
   dim3 grid(a.splits, a.num_kv_heads, a.batch);
   decode_split_kernel<G, FUSED><<<grid, pkv_host::kDecodeWarps * 32, smem, s>>>(a);
   return cudaGetLastError();
@@ -927,13 +923,9 @@ cudaError_t launch_split(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
 
 template <int G, bool FUSED>
 cudaError_t launch_i8mma_as(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_i8mma_kernel<G, FUSED>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, i8mma::SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = pkv_host::set_max_dynamic_smem(
+      reinterpret_cast<const void*>(decode_split_i8mma_kernel<G, FUSED>), i8mma::SMEM);
+  if (e != cudaSuccess) return e;
   if ((long long)a.num_pages * a.num_kv_heads * kPageSize >= (1ll << 31))
     return cudaErrorNotSupported;
   CUtensorMap tk, tv;

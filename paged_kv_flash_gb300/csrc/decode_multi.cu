@@ -464,13 +464,9 @@ namespace pkv_host {
 
 cudaError_t launch_decode_multi(const MultiLaunch& a, cudaStream_t s) {
   if (a.batch == 0 || a.total_q == 0) return cudaSuccess;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_multi_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  cudaError_t e = pkv_host::set_max_dynamic_smem(
+      reinterpret_cast<const void*>(decode_multi_kernel), SMEM);
+  if (e != cudaSuccess) return e;
   if ((long long)a.num_pages * a.num_kv_heads * kPageSize >= (1ll << 31))
     return cudaErrorNotSupported;
   CUtensorMap tk, tv;
@@ -479,7 +475,7 @@ cudaError_t launch_decode_multi(const MultiLaunch& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   dim3 grid(a.splits, a.num_kv_heads * a.row_groups, a.batch);
   decode_multi_kernel<<<grid, kThreads, SMEM, s>>>(tk, tv, a);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
   decode_multi_combine_kernel<<<a.total_q * a.num_q_heads, 128, 0, s>>>(a);
   return cudaGetLastError();

@@ -1329,14 +1329,9 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
       !encode_pool_map(&tv, a.v, a.num_pages, a.num_kv_heads) ||
       !encode_q_map(&tq, a.q, a.total_q, a.num_q_heads))
     return cudaErrorInvalidValue;
-  static bool configured = false;
-  if (!configured) {
-    for (auto fn : {prefill_kernel<false>, prefill_kernel<true>}) {
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           SMEM_BYTES);
-      if (e != cudaSuccess) return e;
-    }
-    configured = true;
+  for (auto fn : {prefill_kernel<false>, prefill_kernel<true>}) {
+    cudaError_t e = pkv_host::set_max_dynamic_smem(reinterpret_cast<const void*>(fn), SMEM_BYTES);
+    if (e != cudaSuccess) return e;
   }
   if (a.ctas <= 0 || a.ctas > kMaxPrefillCtas || !a.workspace) return cudaErrorInvalidValue;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
