@@ -38,15 +38,17 @@ sys.path.insert(0, ROOT)
 
 from paged_kv_flash_gb300 import workloads as W  # noqa: E402
 
-# DRAM bytes (read + write) per prefill launch of the mixed step, from one ncu
-# capture of `bench.py --profile-case prefill_chunk` (2,048 rows against
-# 16,384 positions: 142.5 MB, profiles/prefill_kernel_chunk2048_ctx16384.md),
-# scaled to the mixed step's average context per launch (15,235 positions):
-# K/V traffic grows with the context a chunk attends to.  Re-measure (or set
-# to None) whenever the prefill kernel changes.
-PREFILL_TRAFFIC_BYTES = 132.5e6
-PREFILL_TRAFFIC_NOTE = ("ncu dram read+write of a 2,048 x 16,384 launch (142.5 MB) scaled by "
-                        "mean context 15,235 / 16,384")
+# Per-launch DRAM traffic and tensor-pipe share of the prefill kernel come from
+# the committed ncu summary below; each figure carries the SHA-256 of the
+# kernel's sources when it was captured, and is reported only while the
+# sources still match (otherwise null: the counters describe another kernel).
+PREFILL_PROFILE = os.path.join(ROOT, "profiles", "prefill_kernel_mixed_step.md")
+PREFILL_SOURCES = [os.path.join(ROOT, "paged_kv_flash_gb300", "csrc", f)
+                   for f in ("prefill.cu", "common.cuh", "internal.h")]
+# Dense bf16 tensor-core peak of one GB300 from NVIDIA's HGX B300 figures:
+# 36 PFLOP/s FP16/BF16 per 8 GPUs, quoted with 2:4 sparsity, so 2.25 PFLOP/s
+# dense per GPU.
+SPEC_BF16_TFLOPS = 2250.0
 
 METRIC = ("decode attn µs & HBM GB/s (% of 8 TB/s); prefill attn TFLOP/s (% of peak)")
 NOMINAL_HBM_GBS = 8000.0
@@ -55,13 +57,46 @@ SCALE = 1.0 / np.sqrt(D)
 
 
 def peaks():
+    """(HBM GB/s, bf16 burst TFLOP/s, bf16 sustained TFLOP/s, source, median SM
+    MHz under load while they were measured or None)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
+        mhz = (p.get("clocks_under_load") or {}).get("sm_mhz_median")
         return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), \
-            "measured"
+            "measured", (float(mhz) if mhz else None)
     except Exception:
-        return 6800.0, 1900.0, 1700.0, "fallback"
+        return 6800.0, 1900.0, 1700.0, "fallback", None
+
+
+def sources_sha256(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def prefill_profile():
+    """Figures of the committed prefill ncu summary whose recorded source hash
+    matches the current prefill sources: {key: float}.  The summary holds
+    lines `key = value  (sha256 <hex>)`."""
+    out = {}
+    try:
+        cur = sources_sha256(PREFILL_SOURCES)
+        with open(PREFILL_PROFILE) as f:
+            for line in f:
+                line = line.strip().strip("`")
+                if " = " not in line or "(sha256 " not in line:
+                    continue
+                key, rest = line.split(" = ", 1)
+                val, sha = rest.split("(sha256 ", 1)
+                if sha.rstrip(")").strip() == cur:
+                    out[key.strip()] = float(val.strip())
+    except (OSError, ValueError):
+        pass
+    return out
 
 
 # ------------------------------------------------------------------ clocks
@@ -246,48 +281,64 @@ def time_mixed(torch, pk, mixed, K, Wu, world, rank):
         dist.barrier()
     clk = clocks.stop()
     assert pk.poll_device_error() == pk.OK, "device-side error in the timed region"
-    total_ms = max_over_ranks(torch, t0.elapsed_time(t1))
+    total_ms = t0.elapsed_time(t1)
     app_ms = pre_ms = dec_ms = 0.0
     flops = dbytes = 0.0
     launches = 0
-    # per chunk of the prompt (step i runs chunk i mod 14): summed times, count
-    per = [[0.0, 0.0, 0.0, 0] for _ in range(nsteps)]
+    # per chunk of the prompt (step i runs chunk i mod 14): summed phase
+    # times, summed step times (from this step's first event to the next
+    # step's), count
+    per = [[0.0, 0.0, 0.0, 0.0, 0] for _ in range(nsteps)]
     for i in range(K):
         e = evs[i]
         c = (Wu + i) % nsteps
         st = mixed.steps[c]
         a, p, d = e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])
+        whole = e[0].elapsed_time(evs[i + 1][0] if i + 1 < K else t1)
         app_ms += a
         pre_ms += p
         dec_ms += d
-        per[c][0] += a
-        per[c][1] += p
-        per[c][2] += d
-        per[c][3] += 1
+        for j, v in enumerate((a, p, d, whole)):
+            per[c][j] += v
+        per[c][4] += 1
         flops += st["flops"]
         dbytes += st["dbytes"]
         launches += st["launches"]
     chunks = []
-    for c, (a, p, d, n) in enumerate(per):
+    for c, (a, p, d, w, n) in enumerate(per):
         if not n:
             continue
         st = mixed.steps[c]
         chunks.append({"chunk": c, "rows": st["chunk_len"], "context": st["context"],
+                       "step_us": round(w * 1e3 / n, 2),
                        "append_us": round(a * 1e3 / n, 2), "prefill_us": round(p * 1e3 / n, 2),
                        "prefill_TFLOPs": round(st["flops"] / (p * 1e-3 / n) / 1e12, 1),
                        "decode_us": round(d * 1e3 / n, 2),
                        "decode_GBps": round(st["dbytes"] / (d * 1e-3 / n) / 1e9, 1)})
-    return dict(total_ms=total_ms, app_ms=app_ms, pre_ms=pre_ms, dec_ms=dec_ms, flops=flops,
-                dbytes=dbytes, launches=launches, clocks=clk, chunks=chunks)
+    # The step time weighs the 14 chunks equally (the mean over chunks of the
+    # chunk's mean step time), so that it does not depend on which chunks
+    # K steps happen to cover; with K < 14 it is the plain mean.
+    if len(chunks) == nsteps:
+        step_ms = float(np.mean([per[c][3] / per[c][4] for c in range(nsteps)]))
+        balanced = True
+    else:
+        step_ms, balanced = total_ms / K, False
+    step_ms = max_over_ranks(torch, step_ms)
+    total_ms = max_over_ranks(torch, total_ms)
+    return dict(total_ms=total_ms, step_ms=step_ms, balanced=balanced, app_ms=app_ms,
+                pre_ms=pre_ms, dec_ms=dec_ms, flops=flops, dbytes=dbytes, launches=launches,
+                clocks=clk, chunks=chunks)
 
 
-def time_e2e(torch, pk, mixed, K):
-    """Same steps through the public API from pinned host buffers: every step
-    copies its inputs host->device and reads its outputs back.  The copies
-    overlap the kernels, as a serving loop would run them: step i+1's inputs
-    go up on one copy stream while step i computes, and step i's outputs come
-    back on another from one of two output buffers (the compute stream waits
-    for a buffer's read-back before reusing it)."""
+def time_e2e(torch, pk, mixed, K, first):
+    """The steps first .. first + K - 1 (the device-timed steps when K is a
+    whole number of passes over the 14 chunks) through the public API from
+    pinned host buffers: every step copies its inputs host->device and reads
+    its outputs back.  The copies overlap the kernels, as a serving loop
+    would run them: step i+1's inputs go up on one copy stream while step i
+    computes, and step i's outputs come back on another from one of two
+    output buffers (the compute stream waits for a buffer's read-back before
+    reusing it)."""
     host = []
     for st in mixed.steps:
         s = st["host"]
@@ -342,18 +393,18 @@ def time_e2e(torch, pk, mixed, K):
         counts["d2h"] += (n * op.shape[1] * D * 2 + n * lp.shape[1] * 4 + od.numel() * 2 +
                           ld.numel() * 4)
 
-    def loop(n_iter):
-        upload(0)
-        for i in range(n_iter):
-            if i + 1 < n_iter:
+    def loop(start, n_iter):
+        upload(start)
+        for i in range(start, start + n_iter):
+            if i + 1 < start + n_iter:
                 upload(i + 1)
             run(i)
         torch.cuda.synchronize()
 
-    loop(nsteps)                                   # warm-up pass over every chunk
+    loop(first, nsteps)                            # warm-up pass over every chunk
     counts["h2d"] = counts["d2h"] = 0
     t0 = time.perf_counter()
-    loop(K)
+    loop(first, K)
     dt = time.perf_counter() - t0
     return dt * 1e6 / K, counts["h2d"] // K, counts["d2h"] // K
 
@@ -732,6 +783,89 @@ def profile_case(torch, pk, name, reps=3):
     print(json.dumps({"profile_case": name, "us": round(us, 2), unit: round(rate, 1)}))
 
 
+def make_line(K, Wu, world, r, e2e, peaks_, prof, config, nsteps=14):
+    """The JSON line of the mixed-step run from the timings r (time_mixed),
+    the end-to-end result e2e = (us, h2d bytes, d2h bytes, steps), the peaks
+    (peaks()) and the prefill profile figures (prefill_profile())."""
+    hbm, bf16, bf16_sus, peak_src, peak_mhz = peaks_
+    e2e_us, h2d, d2h, K_e2e = e2e
+    us_per_step = r["step_ms"] * 1e3
+    pre_tflops = r["flops"] / (r["pre_ms"] * 1e-3) / 1e12
+    dec_gbs = r["dbytes"] / (r["dec_ms"] * 1e-3) / 1e9
+    # the timed region is short (well under a second at the default steps),
+    # so the kernel runs at burst clocks: the burst peak is the denominator
+    region_s = r["total_ms"] * 1e-3
+    peak, peak_kind = (bf16, "burst") if region_s < 1.0 else (bf16_sus, "sustained")
+    frac = pre_tflops / peak
+    n_pre = K                                        # one prefill launch per step
+    traffic = prof.get("dram_bytes_per_launch_mixed_step")
+    sm_mhz = r["clocks"].get("sm_mhz")
+    roofline = {
+        "kernel": "prefill_kernel (tcgen05)", "bound": "tensor",
+        "achieved": round(pre_tflops, 1), "peak": peak, "unit": "TFLOP/s",
+        "frac": round(frac, 4), "traffic": traffic,
+        "peak_source": (f"{peak_src} bf16 {peak_kind} (MEASURED_PEAKS.json; timed region "
+                        f"{region_s:.3f} s)"),
+        "achieved_note": (f"causal flops 4*D*Hq*keys over the {n_pre} prefill launches / their "
+                          "summed CUDA-event durations in the timed region"),
+        "traffic_note": ("mean dram read+write bytes per prefill launch of the mixed step's 14 "
+                         "chunks, from the committed ncu summary of this kernel's sources"
+                         if traffic is not None else
+                         "null: no ncu capture of the current prefill sources"),
+        "frac_of_spec_dense_bf16": round(pre_tflops / SPEC_BF16_TFLOPS, 4),
+        "spec_peak_note": ("2,250 TFLOP/s dense bf16 per GPU: NVIDIA HGX B300 36 PFLOP/s "
+                           "FP16/BF16 per 8 GPUs with 2:4 sparsity, halved"),
+    }
+    if peak_mhz and sm_mhz:
+        roofline["frac_clock_normalized"] = round(pre_tflops / (peak * sm_mhz / peak_mhz), 4)
+        roofline["clock_note"] = (f"peak scaled by bench SM clock {sm_mhz:.0f} MHz / "
+                                  f"{peak_mhz:.0f} MHz median under load when the peaks were "
+                                  "measured")
+    if "tensor_pipe_active_pct_2048x16384" in prof:
+        roofline["ncu_tensor_pipe_active_pct"] = prof["tensor_pipe_active_pct_2048x16384"]
+        roofline["ncu_note"] = ("sm__pipe_tensor_cycles_active of one 2,048-row x 16,384-"
+                                "position launch (same sources)")
+
+    line = {
+        "metric": METRIC, "value": round(us_per_step, 2), "unit": "us", "n_gpus": world,
+        "steps": K, "warmup": Wu, "ms_per_step": round(us_per_step / 1e3, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes of the pages' workloads)", "config": config,
+        "value_note": ("us per step, the 14 prompt chunks weighted equally (mean over chunks of "
+                       "each chunk's mean step time)" if r["balanced"] else
+                       "us per step, plain mean (fewer than 14 steps timed)"),
+        "plain_mean_us": round(r["total_ms"] * 1e3 / K, 2),
+        "decode": {"us_per_step": round(r["dec_ms"] * 1e3 / K, 2), "GBps": round(dec_gbs, 1),
+                   "frac_of_8TBps": round(dec_gbs / NOMINAL_HBM_GBS, 4),
+                   "frac_of_measured": round(dec_gbs / hbm, 4),
+                   "bytes_per_step": round(r["dbytes"] / K)},
+        "prefill": {"us_per_step": round(r["pre_ms"] * 1e3 / K, 2),
+                    "TFLOPs": round(pre_tflops, 1),
+                    "frac_of_measured_burst": round(pre_tflops / bf16, 4),
+                    "frac_of_measured_sustained": round(pre_tflops / bf16_sus, 4),
+                    "frac_of_spec_dense": round(pre_tflops / SPEC_BF16_TFLOPS, 4),
+                    "flops_per_step": round(r["flops"] / K)},
+        "append": {"us_per_step": round(r["app_ms"] * 1e3 / K, 2)},
+        # the 14 steps of one pass over the prompt (each the mean over the
+        # timed steps that ran that chunk), and their sum
+        "chunk_steps": r["chunks"],
+        "prompt_pass": {"step_us": round(sum(c["step_us"] for c in r["chunks"]), 1),
+                        "prefill_us": round(sum(c["prefill_us"] for c in r["chunks"]), 1),
+                        "decode_us": round(sum(c["decode_us"] for c in r["chunks"]), 1),
+                        "append_us": round(sum(c["append_us"] for c in r["chunks"]), 1),
+                        "chunks": len(r["chunks"])},
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_us, 2), "unit": "us", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "steps": K_e2e,
+                "note": (f"steps {Wu}..{Wu + K_e2e - 1} (whole passes over the 14 chunks) through "
+                         "the public API, inputs from pinned host memory each step, outputs read "
+                         "back each step; wall clock")},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    return line
+
+
 # ---------------------------------------------------------------- main
 
 def main(argv=None):
@@ -776,11 +910,17 @@ def main(argv=None):
         for i in range(K):
             c = (Wu + i) % nsteps
             e, dt = oracle_step_sample(wl, c, 4, 2, rng, nthreads)
-            ests.append(e)
+            ests.append((c, e))
             spent += dt
             if spent > 150.0:
                 break
-        v = float(np.mean(ests)) * 1e6
+        per = {}
+        for c, e in ests:
+            per.setdefault(c, []).append(e)
+        # the 14 chunks weighted equally when every chunk was sampled, as in
+        # the GPU arm's value; otherwise the plain mean
+        v = (float(np.mean([np.mean(x) for x in per.values()])) if len(per) == nsteps
+             else float(np.mean([e for _, e in ests]))) * 1e6
         line = {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": "us",
                 "n_gpus": args.gpus, "steps": len(ests), "warmup": Wu,
                 "ms_per_step": round(v / 1e3, 3), "higher_is_better": False, "scaling": "weak",
@@ -808,50 +948,16 @@ def main(argv=None):
     if args.profile_case:
         profile_case(torch, pk, args.profile_case)
         return 0
-    hbm, bf16, bf16_sus, peak_src = peaks()
+    hbm, bf16, bf16_sus, peak_src, peak_mhz = peaks()
     mixed = Mixed(torch, pk)
     r = time_mixed(torch, pk, mixed, K, Wu, world, rank)
-    e2e_us, h2d, d2h = time_e2e(torch, pk, mixed, min(K, 140))
+    nsteps = len(mixed.steps)
+    K_e2e = -(-K // nsteps) * nsteps               # whole passes over the 14 chunks
+    e2e_us, h2d, d2h = time_e2e(torch, pk, mixed, K_e2e, Wu)
 
-    us_per_step = r["total_ms"] * 1e3 / K
-    pre_tflops = r["flops"] / (r["pre_ms"] * 1e-3) / 1e12
-    dec_gbs = r["dbytes"] / (r["dec_ms"] * 1e-3) / 1e9
-    frac = pre_tflops / bf16_sus
-
-    line = {
-        "metric": METRIC, "value": round(us_per_step, 2), "unit": "us", "n_gpus": world,
-        "steps": K, "warmup": Wu, "ms_per_step": round(us_per_step / 1e3, 4),
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded; shapes of the pages' workloads)", "config": config,
-        "decode": {"us_per_step": round(r["dec_ms"] * 1e3 / K, 2), "GBps": round(dec_gbs, 1),
-                   "frac_of_8TBps": round(dec_gbs / NOMINAL_HBM_GBS, 4),
-                   "frac_of_measured": round(dec_gbs / hbm, 4),
-                   "bytes_per_step": round(r["dbytes"] / K)},
-        "prefill": {"us_per_step": round(r["pre_ms"] * 1e3 / K, 2),
-                    "TFLOPs": round(pre_tflops, 1),
-                    "frac_of_measured_sustained": round(frac, 4),
-                    "frac_of_measured_burst": round(pre_tflops / bf16, 4),
-                    "flops_per_step": round(r["flops"] / K)},
-        "append": {"us_per_step": round(r["app_ms"] * 1e3 / K, 2)},
-        # the 14 steps of one pass over the prompt (each the mean over the
-        # timed steps that ran that chunk), and their sum
-        "steps": r["chunks"],
-        "prompt_pass": {"prefill_us": round(sum(c["prefill_us"] for c in r["chunks"]), 1),
-                        "decode_us": round(sum(c["decode_us"] for c in r["chunks"]), 1),
-                        "append_us": round(sum(c["append_us"] for c in r["chunks"]), 1),
-                        "chunks": len(r["chunks"])},
-        "roofline": {"kernel": "prefill_kernel (tcgen05)", "bound": "tensor",
-                     "achieved": round(pre_tflops, 1), "peak": bf16_sus, "unit": "TFLOP/s",
-                     "frac": round(frac, 4), "traffic": PREFILL_TRAFFIC_BYTES,
-                     "traffic_note": PREFILL_TRAFFIC_NOTE,
-                     "peak_source": f"{peak_src} bf16 sustained (MEASURED_PEAKS.json)",
-                     "achieved_note": ("causal flops 4*D*Hq*keys per launch / CUDA-event "
-                                       "duration of the prefill launches in the timed region")},
-        "e2e": {"value": round(e2e_us, 2), "unit": "us", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": r["launches"],
-        "clocks": r["clocks"],
-    }
+    e2e = (e2e_us, h2d, d2h, K_e2e)
+    line = make_line(K, Wu, world, r, e2e, (hbm, bf16, bf16_sus, peak_src, peak_mhz),
+                     prefill_profile(), config, nsteps)
     if rank == 0 and world == 1 and not args.no_configs:
         line["configs"] = other_configs(torch, pk, hbm, bf16)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
