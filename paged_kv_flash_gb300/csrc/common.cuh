@@ -171,6 +171,33 @@ __device__ __forceinline__ float fast_log2(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// ------------------------------------------- warp-level bf16 tensor MMAs
+
+// D += A B, m16n8k16, bf16 inputs, fp32 accumulate.  Fragments (r = lane / 4,
+// qd = lane % 4): A rows r and r + 8, columns 2qd, 2qd + 1 (a0, a1) and
+// 2qd + 8, 2qd + 9 (a2, a3); B rows 2qd, 2qd + 1 (b0) and + 8 (b1) of column
+// r; D rows r (d0, d1) and r + 8 (d2, d3), columns 2qd, 2qd + 1.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four 8 x 8 b16 matrices from shared memory; lanes 8i .. 8i + 7 give the
+// row addresses of matrix i (16 bytes each).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
+// The same, each matrix transposed.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
 // ------------------------------------------------- split merge
 
 // Log-sum-exp merge of n split partials of one (row, head) by a CTA of 128

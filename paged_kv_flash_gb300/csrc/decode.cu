@@ -4,27 +4,15 @@
 // table, split-KV for decode, and a combine kernel kept separate from the
 // split kernel; "INT8 KV cache": dequantisation inside attention).
 //
-// Two split kernels: decode_split_kernel (bf16 pools, CUDA cores) and
-// decode_split_i8mma_kernel (INT8 pools, warp-level tensor-core MMAs; see
-// its own comment further down).  Both run one CTA per (split, KV head,
-// sequence), 4 warps, and share the warp merge and the combine.
-//
-// bf16 split kernel: one CTA per (split, KV head, sequence), 4 warps.  A split is
-// a run of consecutive logical pages of one sequence; the warps take its
-// pages round-robin and each warp streams its pages through a private ring
-// of shared-memory page buffers filled by the TMA engine (cp.async.bulk of
-// the contiguous 4 KiB (page, head) slabs, L2 evict-first), so no CTA-wide
-// barrier sits in the page loop.  Every warp serves all G query heads of
-// the KV head, so each K/V byte is read from HBM once per decode step.
-//
-// Lane layout inside a warp: DL lanes cover one key's 128 channels (DPL
-// channels each), KG = 32 / DL keys per pass, 16 / KG passes per page.
-// Partial dot products are reduced across the DL lanes with a reduce-scatter
-// (each stage halves the heads a lane carries), so after log2(DL) shuffle
-// stages every lane holds one head's score of its key.  The online-softmax
-// state of a head lives in the lanes that own it; p and the rescale factor
-// reach the other lanes by shuffles.  Shared-memory reads rotate their
-// 16-byte chunk order by key so that a warp's 32 loads hit all 32 banks.
+// Two split kernels: decode_split_kernel (bf16 pools) and
+// decode_split_i8mma_kernel (INT8 pools), both on warp-level tensor-core
+// MMAs (see their own comments further down).  Both run one CTA per (split,
+// KV head, sequence); a split is a run of consecutive logical pages of one
+// sequence, its warps take the pages round-robin and each warp streams its
+// pages through a private ring of shared-memory page buffers filled by the
+// TMA engine (L2 evict-first), so no CTA-wide barrier sits in the page loop.
+// Every warp serves all G query heads of the KV head, so each K/V byte is
+// read from HBM once per decode step.
 //
 // The split's result is normalised (O / l) and written with its log2-domain
 // lse; with a single split the kernel writes the bf16 output directly and
@@ -44,154 +32,65 @@ using namespace pkv;
 
 __device__ uint32_t g_err_decode;
 
-template <int G>
-struct Cfg {
-  static constexpr int DL = (G <= 2) ? 4 : (G == 4 ? 8 : 16);    // lanes per key
-  static constexpr int KG = 32 / DL;                              // keys per pass
-  static constexpr int PASSES = kPageSize / KG;
-  static constexpr int DPL = kHeadDim / DL;                       // channels per lane
-  static constexpr int LDB = 16;                                  // bytes per shared load
-  static constexpr int EPL = 8;                                   // bf16 elements per load
-  static constexpr int NLD = DPL / EPL;                           // loads per lane per key
-  static constexpr int ROWB = kHeadDim * 2;                       // bytes per key row
-  static constexpr int SLAB = kPageSize * ROWB;                   // K or V slab bytes
-  static constexpr int BUF = 2 * SLAB;                            // one page of K and V
-  static constexpr int HL = DL / G;                               // lanes per head after scatter
-  static constexpr int NBUF = 3;                                  // page buffers per warp
-  static_assert(NLD >= 1 && (NLD & (NLD - 1)) == 0, "loads per key must be a power of two");
-  static_assert(BUF % 128 == 0, "page buffers stay 128-byte aligned");
-};
+// ------------------------------------------------------------------------
+// bf16 split kernel on tensor cores (mma.sync m16n8k16, bf16 in, fp32 out).
+//
+// A warp takes whole 16-key pages of its split (round-robin over the CTA's
+// warps) from a private ring of shared-memory buffers that the TMA engine
+// fills (K and V slabs as 16-row x 64-channel boxes, 128-byte swizzled, L2
+// evict-first), so no CTA-wide barrier sits in the page loop.  Per page:
+//   S^T = K Q^T: A = the page's 16 keys (ldmatrix), B = the G query rows of
+//        the KV head as columns (bf16, exact, in registers); 8 channel steps
+//        in two accumulators.  Lane (r, qd) gets keys r and r + 8 of heads
+//        2qd and 2qd + 1, so the running max, sum and the O columns of a
+//        head live in the lanes that own it (no shuffles but the page max);
+//   O^T += V^T P^T: A = V^T (ldmatrix.trans), B = P (rounded to bf16) moved
+//        from the key-major layout of S^T to the head-major B fragment by
+//        two register transposes (movmatrix); 8 channel tiles.
+// 16 MMAs per page instead of ~1,000 FMAs and shuffles on CUDA cores.  Slots
+// past the sequence's end get p = 0 and their V values are zeroed before
+// the MMA (0 x NaN would reach O).
+namespace bfmma {
 
-// Loads 8 consecutive bf16 at a shared address as four fp32 pairs.
-__device__ __forceinline__ void load_widen(const uint8_t* p, float2 (&x)[4]) {
-  const uint4 r = *reinterpret_cast<const uint4*>(p);
-  x[0] = make_float2(bf16lo(r.x), bf16hi(r.x));
-  x[1] = make_float2(bf16lo(r.y), bf16hi(r.y));
-  x[2] = make_float2(bf16lo(r.z), bf16hi(r.z));
-  x[3] = make_float2(bf16lo(r.w), bf16hi(r.w));
+constexpr int W = pkv_host::kDecodeWarps;               // warps per CTA, pages round-robin
+constexpr int NB = 3;                                   // page buffers per warp
+constexpr int HALF = kPageSize * 128;                   // one box: 16 keys x 64 bf16
+constexpr int SLAB = 2 * HALF;                          // K or V of one (page, head)
+constexpr int PAGE = 2 * SLAB;                          // K, then V
+constexpr int WARP_BYTES = NB * PAGE;
+constexpr int SMEM = 1024 + W * WARP_BYTES;
+static_assert(W * NB * 8 <= 1016, "barriers fit the header");
+
+// The 16-byte chunk holding channels ch .. ch + 7 of key row `key` of a slab:
+// two 64-channel halves, chunk c of row k at c ^ (k & 7).
+__device__ __forceinline__ uint32_t slab_chunk(uint32_t slab, int key, int ch) {
+  const int half = ch >> 6, c = (ch & 63) >> 3;
+  return slab + half * HALF + key * 128 + ((c ^ (key & 7)) << 4);
 }
 
-// Sum of v[g] over the DL lanes of a key, scattered: afterwards lane dl holds
-// the full sum of head dl / (DL / G).
-template <int G, int DL>
-__device__ __forceinline__ float reduce_scatter(float (&v)[G], int dl) {
-  int nv = G;
-#pragma unroll
-  for (int m = DL / 2; m >= 1; m >>= 1) {
-    const bool upper = (dl & m) != 0;
-    if (nv > 1) {
-#pragma unroll
-      for (int i = 0; i < G / 2; ++i) {
-        if (i < nv / 2) {
-          const float send = upper ? v[i] : v[i + nv / 2];
-          const float keep = upper ? v[i + nv / 2] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-        }
-      }
-      nv >>= 1;
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
-    }
-  }
-  return v[0];
+// An 8 x 8 b16 matrix held one row per 4 lanes, transposed across the warp.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
 }
 
-template <int G>
-struct WarpState {
-  using C = Cfg<G>;
-  float2 q[C::NLD][C::EPL / 2][G];   // pre-scaled query, in this lane's chunk order
-  float2 o[C::NLD][C::EPL / 2][G];   // unnormalised output accumulators
-  float m = -INFINITY;               // running max (log2 domain) of head dl / HL
-  float l = 0.f;                     // partial sum of head dl / HL over this lane's keys
-};
-
-// One page of 16 keys (nvalid of them real) from shared memory.
-template <int G, bool PARTIAL>
-__device__ __forceinline__ void process_page(WarpState<G>& st, const uint8_t* buf,
-                                             int nvalid, int kg, int dl) {
-  using C = Cfg<G>;
-  const uint8_t* kbuf = buf;
-  const uint8_t* vbuf = buf + C::SLAB;
-  const int lane = kg * C::DL + dl;
-
-  float s[C::PASSES];
-#pragma unroll
-  for (int ps = 0; ps < C::PASSES; ++ps) {
-    const int key = ps * C::KG + kg;
-    const uint8_t* row = kbuf + key * C::ROWB + dl * C::DPL * 2;
-    float2 acc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < C::NLD; ++j) {
-      const int jj = (j + kg) & (C::NLD - 1);
-      float2 x[C::EPL / 2];
-      load_widen(row + jj * C::LDB, x);
-#pragma unroll
-      for (int i = 0; i < C::EPL / 2; ++i)
-#pragma unroll
-        for (int g = 0; g < G; ++g) acc[g] = fma2(st.q[j][i][g], x[i], acc[g]);
-    }
-    float part[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) part[g] = acc[g].x + acc[g].y;
-    const float sc = reduce_scatter<G, C::DL>(part, dl);
-    s[ps] = (PARTIAL && key >= nvalid) ? -INFINITY : sc;
-  }
-
-  float pm = s[0];
-#pragma unroll
-  for (int ps = 1; ps < C::PASSES; ++ps) pm = fmaxf(pm, s[ps]);
-#pragma unroll
-  for (int m = C::DL; m < 32; m <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, m));
-  const float m_new = fmaxf(st.m, pm);
-  const float alpha = fast_exp2(st.m - m_new);
-  float p[C::PASSES];
-  float lsum = 0.f;
-#pragma unroll
-  for (int ps = 0; ps < C::PASSES; ++ps) {
-    p[ps] = fast_exp2(s[ps] - m_new);
-    lsum += p[ps];
-  }
-  st.l = st.l * alpha + lsum;
-  st.m = m_new;
-
-  if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float ag = __shfl_sync(0xffffffffu, alpha, g * C::HL);
-      const float2 a2 = make_float2(ag, ag);
-#pragma unroll
-      for (int j = 0; j < C::NLD; ++j)
-#pragma unroll
-        for (int i = 0; i < C::EPL / 2; ++i) st.o[j][i][g] = mul2(st.o[j][i][g], a2);
-    }
-  }
-
-#pragma unroll
-  for (int ps = 0; ps < C::PASSES; ++ps) {
-    const int key = ps * C::KG + kg;
-    float pg[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      pg[g] = __shfl_sync(0xffffffffu, p[ps], (lane & ~(C::DL - 1)) | (g * C::HL));
-    if (!PARTIAL || key < nvalid) {
-      const uint8_t* row = vbuf + key * C::ROWB + dl * C::DPL * 2;
-#pragma unroll
-      for (int j = 0; j < C::NLD; ++j) {
-        const int jj = (j + kg) & (C::NLD - 1);
-        float2 x[C::EPL / 2];
-        load_widen(row + jj * C::LDB, x);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float2 p2 = make_float2(pg[g], pg[g]);
-#pragma unroll
-          for (int i = 0; i < C::EPL / 2; ++i) st.o[j][i][g] = fma2(p2, x[i], st.o[j][i][g]);
-        }
-      }
-    }
-  }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
+
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, int x, int row,
+                                        uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(row), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+}  // namespace bfmma
 
 // The CTA's merge of its warps: each warp has parked (O [G][128], m [G],
 // l [G]) at the start of its buffer area (bufs + w * warp_stride, log2
@@ -278,17 +177,18 @@ __device__ __forceinline__ void merge_warps(const pkv_host::DecodeLaunch& a, uin
 // (a.ws_ctr counts them); otherwise a separate combine kernel does.  A
 // template parameter, so that the default kernel carries none of that code.
 template <int G, bool FUSED>
-__global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
-    decode_split_kernel(const __grid_constant__ pkv_host::DecodeLaunch a) {
-  using C = Cfg<G>;
-  constexpr int W = pkv_host::kDecodeWarps;
-  constexpr int NBUF = C::NBUF;
+__global__ void __launch_bounds__(bfmma::W * 32, 2)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tk,
+                        const __grid_constant__ CUtensorMap tv,
+                        const __grid_constant__ pkv_host::DecodeLaunch a) {
+  using namespace bfmma;
+  constexpr uint32_t FULL = 0xffffffffu;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* bufs = smem + 1024;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kg = lane / C::DL, dl = lane % C::DL;
+  const int r = lane >> 2, qd = lane & 3;
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int Hq = a.num_q_heads;
 
@@ -306,30 +206,26 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
   const int p_end = min(npages, p_begin + a.pages_per_split);
   const int n_w = max(0, (p_end - p_begin - warp + W - 1) / W);   // pages of this warp
 
-  const uint32_t bar0 = smem_u32(bars + warp * NBUF);
-  uint8_t* wbuf = bufs + (size_t)warp * NBUF * C::BUF;
+  const uint32_t bar0 = smem_u32(bars + warp * NB);
+  uint8_t* wbuf = bufs + (size_t)warp * WARP_BYTES;
   const uint32_t wbuf_s = smem_u32(wbuf);
   if (lane == 0) {
 #pragma unroll
-    for (int k = 0; k < NBUF; ++k) mbar_init(bar0 + 8 * k, 1);
+    for (int k = 0; k < NB; ++k) mbar_init(bar0 + 8 * k, 1);
     fence_mbar_init();
   }
   __syncwarp();
 
-  const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
-  const size_t Hkv = (size_t)a.num_kv_heads;
-  const uint8_t* kpool = static_cast<const uint8_t*>(a.k);
-  const uint8_t* vpool = static_cast<const uint8_t*>(a.v);
-  const uint64_t policy = l2_policy_evict_first();
-
   // Page ids of this warp's pages, 32 at a time, one per lane.
+  const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
+  const uint64_t policy = l2_policy_evict_first();
   int bt_cache = 0;
   auto page_id = [&](int i) -> int {
     if ((i & 31) == 0) {
       const int lp = p_begin + warp + (i + lane) * W;
       bt_cache = (i + lane < n_w) ? __ldg(bt_row + lp) : 0;
     }
-    int pg = __shfl_sync(0xffffffffu, bt_cache, i & 31);
+    int pg = __shfl_sync(FULL, bt_cache, i & 31);
     if (pg < 0 || pg >= a.num_pages) {
       if (lane == 0) atomicOr(&g_err_decode, kErrBadIndex);
       pg = 0;
@@ -338,64 +234,134 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
   };
   auto issue = [&](int i, int pg) {
     if (lane == 0) {
-      const int k = i % NBUF;
-      const uint32_t bar = bar0 + 8 * k;
-      const uint32_t dst = wbuf_s + k * C::BUF;
-      const size_t slab = (size_t)pg * Hkv + h;
+      const int k = i % NB;
+      const uint32_t bar = bar0 + 8 * k, dst = wbuf_s + k * PAGE;
+      const int row = (pg * a.num_kv_heads + h) * kPageSize;
       // the warp's generic-proxy reads of this buffer are done (__syncwarp);
       // order them before the async-proxy refill
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(bar, C::BUF);
-      bulk_g2s_hint(dst, kpool + slab * C::SLAB, C::SLAB, bar, policy);
-      bulk_g2s_hint(dst + C::SLAB, vpool + slab * C::SLAB, C::SLAB, bar, policy);
+      mbar_arrive_expect_tx(bar, PAGE);
+      tma_box(dst, &tk, 0, row, bar, policy);
+      tma_box(dst + HALF, &tk, 64, row, bar, policy);
+      tma_box(dst + SLAB, &tv, 0, row, bar, policy);
+      tma_box(dst + SLAB + HALF, &tv, 64, row, bar, policy);
     }
   };
-
-  // Page ids are needed in issue order 0, 1, 2, ...; the prologue issues the
-  // first NBUF pages, the loop refills buffer k after consuming page i.
-  const int pro = min(NBUF, n_w);
+  // the first page copies go out before the query rows are loaded
+  const int pro = min(NB, n_w);
   for (int i = 0; i < pro; ++i) issue(i, page_id(i));
   int issued = pro;
-  // Query rows of the group, pre-scaled by softmax_scale * log2(e).  Loaded
-  // after the first page copies are in flight, so their latency overlaps.
-  WarpState<G> st;
+
+  // The query rows as B fragments: column r = head r of the group (zero for
+  // r >= G), rows = channels 16 ks + 2qd, + 1 (qb[ks][0]) and + 8, + 9.
+  uint32_t qb[8][2];
   {
-    const float qs = a.softmax_scale * kLog2e;
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+    const bool valid = r < G;
+    const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
+                                ((size_t)b * Hq + h * G + (valid ? r : 0)) * kHeadDim;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const __nv_bfloat16* qrow = qb + ((size_t)b * Hq + h * G + g) * kHeadDim;
-#pragma unroll
-      for (int j = 0; j < C::NLD; ++j) {
-        const int jj = (j + kg) & (C::NLD - 1);
-        const int d0 = dl * C::DPL + jj * C::EPL;      // a whole 16-byte chunk
-        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qrow + d0));
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          st.q[j][e][g] = make_float2(bf16lo(w[e]) * qs, bf16hi(w[e]) * qs);
-          st.o[j][e][g] = make_float2(0.f, 0.f);
-        }
-      }
+    for (int ks = 0; ks < 8; ++ks) {
+      qb[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * qd)) : 0u;
+      qb[ks][1] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * qd))
+                        : 0u;
     }
   }
+  const float sl2 = a.softmax_scale * kLog2e;
+  // O^T: channels 16 mt + r (o[mt][0..1]) and + 8 (o[mt][2..3]) of heads 2qd
+  // (o[mt][0], o[mt][2]) and 2qd + 1 (o[mt][1], o[mt][3])
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[mt][j] = 0.f;
+  // per head 2qd + e: the max the exponentials are taken against (log2
+  // domain) and this lane's part of the sum
+  float mu[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  // this lane's ldmatrix rows: K (keys, non-transposed) and V (transposed)
+  const int k_key = (lane & 7) + 8 * ((lane >> 3) & 1), k_ch = 8 * (lane >> 4);
+  const int v_key = (lane & 7) + 8 * (lane >> 4), v_ch = 8 * ((lane >> 3) & 1);
 
   bool failed = false;
   int i_fail = 0;
   for (int i = 0; i < n_w; ++i) {
-    const int k = i % NBUF;
-    if (!mbar_wait(bar0 + 8 * k, (uint32_t)(i / NBUF) & 1u)) {
+    const int k = i % NB;
+    if (!mbar_wait(bar0 + 8 * k, (uint32_t)(i / NB) & 1u)) {
       failed = true;
       i_fail = i;
       break;
     }
     const int lp = p_begin + warp + i * W;
     const int nvalid = min(kPageSize, L - lp * kPageSize);
-    const uint8_t* buf = wbuf + k * C::BUF;
-    if (nvalid == kPageSize)
-      process_page<G, false>(st, buf, nvalid, kg, dl);
-    else
-      process_page<G, true>(st, buf, nvalid, kg, dl);
+    const uint32_t kst = wbuf_s + k * PAGE, vst = kst + SLAB;
+
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ks += 2) {
+      uint32_t ka[4], kb[4];
+      ldsm_x4(slab_chunk(kst, k_key, 16 * ks + k_ch), ka);
+      ldsm_x4(slab_chunk(kst, k_key, 16 * ks + 16 + k_ch), kb);
+      mma_bf16(d0, ka, qb[ks][0], qb[ks][1]);
+      mma_bf16(d1, kb, qb[ks + 1][0], qb[ks + 1][1]);
+    }
+    // scores (unscaled): key r of heads 2qd, 2qd + 1 (s[0], s[1]), key r + 8 (s[2], s[3])
+    float s[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[e] = d0[e] + d1[e];
+    if (nvalid < kPageSize) {
+      if (r >= nvalid) s[0] = s[1] = -INFINITY;
+      if (r + 8 >= nvalid) s[2] = s[3] = -INFINITY;
+    }
+    float pm[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+#pragma unroll
+    for (int x = 4; x <= 16; x <<= 1) {
+      pm[0] = fmaxf(pm[0], __shfl_xor_sync(FULL, pm[0], x));
+      pm[1] = fmaxf(pm[1], __shfl_xor_sync(FULL, pm[1], x));
+    }
+    // the max moves only when the page max passes it by more than 2^8
+    // (p <= 256; exact: l and O share it)
+    float alpha[2] = {1.f, 1.f};
+    bool grow = false;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float m_pg = pm[e] * sl2;
+      if (m_pg > mu[e] + 8.f) {
+        alpha[e] = fast_exp2(mu[e] - m_pg);
+        mu[e] = m_pg;
+        l[e] *= alpha[e];
+        grow = true;
+      }
+    }
+    if (__any_sync(FULL, grow)) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= alpha[0];
+        o[mt][2] *= alpha[0];
+        o[mt][1] *= alpha[1];
+        o[mt][3] *= alpha[1];
+      }
+    }
+    const float p0 = fast_exp2(fmaf(s[0], sl2, -mu[0])), p1 = fast_exp2(fmaf(s[1], sl2, -mu[1]));
+    const float p2 = fast_exp2(fmaf(s[2], sl2, -mu[0])), p3 = fast_exp2(fmaf(s[3], sl2, -mu[1]));
+    l[0] += p0 + p2;
+    l[1] += p1 + p3;
+    // P as the B fragment of O^T += V^T P^T: head r, keys 2qd, 2qd + 1 (+ 8)
+    const uint32_t pb0 = movm_t(pack_bf16x2(p0, p1));
+    const uint32_t pb1 = movm_t(pack_bf16x2(p2, p3));
+    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;   // V of slots past the sequence -> 0
+    if (nvalid < kPageSize) {
+      mlo = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+      mhi = (2 * qd + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t va[4];
+      ldsm_x4_t(slab_chunk(vst, v_key, 16 * mt + v_ch), va);
+      va[0] &= mlo;
+      va[1] &= mlo;
+      va[2] &= mhi;
+      va[3] &= mhi;
+      mma_bf16(o[mt], va, pb0, pb1);
+    }
     __syncwarp();
     if (issued < n_w) {
       issue(issued, page_id(issued));
@@ -404,79 +370,40 @@ __global__ void __launch_bounds__(pkv_host::kDecodeWarps * 32)
   }
   if (failed) {
     if (lane == 0) atomicOr(&g_err_decode, kErrTimeout);
-    // Let every copy this warp issued land (bounded) before the buffers are
-    // reused or the CTA exits.
+    // let every copy this warp issued land (bounded) before the buffers are
+    // reused or the CTA exits
     for (int i = i_fail; i < issued; ++i)
-      (void)mbar_wait(bar0 + 8 * (i % NBUF), (uint32_t)(i / NBUF) & 1u);
-    st.m = -INFINITY;
-    st.l = 0.f;
+      (void)mbar_wait(bar0 + 8 * (i % NB), (uint32_t)(i / NB) & 1u);
   }
+  __syncwarp();
 
-  // Warp merge: lanes of different key groups hold the same channels, but
-  // in rotated chunk order (slot j holds chunk (j + kg) mod NLD); put every
-  // lane back in natural order, then sum over the key groups.
-  float l = st.l;
+  // Park (O unnormalised, m, l) of the warp's G heads in its buffers (all of
+  // its copies have landed), then merge the warps.
 #pragma unroll
-  for (int m = C::DL; m < 32; m <<= 1) l += __shfl_xor_sync(0xffffffffu, l, m);
-  if constexpr (C::NLD > 1) {
-    float2 nat[C::NLD][C::EPL / 2][G];
-#pragma unroll
-    for (int c = 0; c < C::NLD; ++c)
-#pragma unroll
-      for (int i = 0; i < C::EPL / 2; ++i)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float2 v = st.o[0][i][g];
-#pragma unroll
-          for (int j = 1; j < C::NLD; ++j)
-            if (((j + kg) & (C::NLD - 1)) == c) v = st.o[j][i][g];
-          nat[c][i][g] = v;
-        }
-#pragma unroll
-    for (int c = 0; c < C::NLD; ++c)
-#pragma unroll
-      for (int i = 0; i < C::EPL / 2; ++i)
-#pragma unroll
-        for (int g = 0; g < G; ++g) st.o[c][i][g] = nat[c][i][g];
+  for (int x = 4; x <= 16; x <<= 1) {
+    l[0] += __shfl_xor_sync(FULL, l[0], x);
+    l[1] += __shfl_xor_sync(FULL, l[1], x);
   }
-#pragma unroll
-  for (int j = 0; j < C::NLD; ++j)
-#pragma unroll
-    for (int i = 0; i < C::EPL / 2; ++i)
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float2 v = st.o[j][i][g];
-#pragma unroll
-        for (int m = C::DL; m < 32; m <<= 1) {
-          v.x += __shfl_xor_sync(0xffffffffu, v.x, m);
-          v.y += __shfl_xor_sync(0xffffffffu, v.y, m);
-        }
-        st.o[j][i][g] = v;
-      }
-
-  // Each warp parks (m, l, O) of its G heads in its own buffers (all of its
-  // copies have landed), then the CTA merges the warps.
   float* wo = reinterpret_cast<float*>(wbuf);              // [G][128]
   float* wm = wo + G * kHeadDim;                           // [G]
   float* wl = wm + G;                                      // [G]
-  if (kg == 0) {
 #pragma unroll
-    for (int j = 0; j < C::NLD; ++j)
+  for (int e = 0; e < 2; ++e) {
+    const int g = 2 * qd + e;
+    if (g < G) {
 #pragma unroll
-      for (int i = 0; i < C::EPL / 2; ++i)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const int d = dl * C::DPL + j * C::EPL + 2 * i;   // natural chunk order
-          *reinterpret_cast<float2*>(wo + g * kHeadDim + d) =
-              failed ? make_float2(0.f, 0.f) : st.o[j][i][g];
-        }
-    if (dl % C::HL == 0) {
-      wm[dl / C::HL] = st.m;
-      wl[dl / C::HL] = failed ? 0.f : l;
+      for (int mt = 0; mt < 8; ++mt) {
+        wo[g * kHeadDim + 16 * mt + r] = failed ? 0.f : o[mt][e];
+        wo[g * kHeadDim + 16 * mt + r + 8] = failed ? 0.f : o[mt][2 + e];
+      }
+      if (r == 0) {
+        wm[g] = failed ? -INFINITY : mu[e];
+        wl[g] = failed ? 0.f : l[e];
+      }
     }
   }
   __syncthreads();
-  merge_warps<G, FUSED>(a, smem, bufs, (size_t)NBUF * C::BUF, split, h, b, nv, direct);
+  merge_warps<G, FUSED, W>(a, smem, bufs, (size_t)WARP_BYTES, split, h, b, nv, direct);
 }
 
 // ------------------------------------------------------------------------
@@ -906,13 +833,17 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_consta
 
 template <int G, bool FUSED>
 cudaError_t launch_split_as(const pkv_host::DecodeLaunch& a, cudaStream_t s) {
-  using C = Cfg<G>;
-  constexpr int smem = 1024 + pkv_host::kDecodeWarps * C::NBUF * C::BUF;
   cudaError_t e = pkv_host::set_max_dynamic_smem(
-      reinterpret_cast<const void*>(decode_split_kernel<G, FUSED>), smem);
+      reinterpret_cast<const void*>(decode_split_kernel<G, FUSED>), bfmma::SMEM);
   if (e != cudaSuccess) return e;
+  if ((long long)a.num_pages * a.num_kv_heads * kPageSize >= (1ll << 31))
+    return cudaErrorNotSupported;
+  CUtensorMap tk, tv;
+  if (!pkv_host::encode_bf16_pool_map(&tk, a.k, a.num_pages, a.num_kv_heads) ||
+      !pkv_host::encode_bf16_pool_map(&tv, a.v, a.num_pages, a.num_kv_heads))
+    return cudaErrorInvalidValue;
   dim3 grid(a.splits, a.num_kv_heads, a.batch);
-  decode_split_kernel<G, FUSED><<<grid, pkv_host::kDecodeWarps * 32, smem, s>>>(a);
+  decode_split_kernel<G, FUSED><<<grid, bfmma::W * 32, bfmma::SMEM, s>>>(tk, tv, a);
   return cudaGetLastError();
 }
 
