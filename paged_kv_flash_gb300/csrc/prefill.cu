@@ -279,6 +279,23 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   return __all_sync(0xffffffffu, ok);
 }
 
+// The same wait for a single thread (no warp vote).
+__device__ __forceinline__ bool wait_bar1(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1u;
+        atomicOr(&g_err_prefill, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Adds to a counter in global memory after every write this thread has seen
 // (including other threads' writes ordered before it by a CTA barrier).
 __device__ __forceinline__ void red_release_add(uint32_t* ctr, uint32_t v) {
@@ -854,6 +871,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------- MMA issuer
+    // One thread (lane 0) runs this role; the other lanes wait at the end.
+    // The tensor core takes MMAs only as fast as this thread issues them, so
+    // nothing between two groups of eight may stall it: no warp votes or
+    // syncs, and as few barrier waits as the dependencies allow.
     // Per segment, iteration j issues PV_A(j-1), QK_A(j), PV_B(j-1), QK_B(j).
     // While softmax A works on S_A(j) the tensor core runs PV_B(j-1) and
     // QK_B(j), and the other way round.  QK_x(j) overwrites S_x, which holds
@@ -862,92 +883,81 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // previous segment's epilogue, which reads O.  K(j) is waited for only
     // after PV_A(j-1) is issued: that PV does not need it and runs while K
     // lands.
-    bool ok = true;
-    int t = 0, cnt_a = 0, cnt_b = 0;
-    for (int sg = 0;; ++sg) {
-      const int ri = sg % NSEG;
-      if (!(ok = wait_bar(bar(BAR_SEGF + ri), (sg / NSEG) & 1, abort_flag))) break;
-      const SegDesc& d = seg_ring[ri];
-      const int end = d.end;
-      const int j0 = d.j0, j1 = d.j1, L = d.L;
-      const int je_a = min(j1, d.nblk_a), je_b = min(j1, d.nblk_b);
-      __syncwarp();
-      if (end) break;
-      if (lane == 0) mbar_arrive(bar(BAR_SEGE + ri));
-      if (!(ok = wait_bar(bar(BAR_QF + 0), sg & 1, abort_flag))) break;
-      if (!(ok = wait_bar(bar(BAR_QF + 1), sg & 1, abort_flag))) break;
-      if (lane == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      int t = 0, cnt_a = 0, cnt_b = 0;
+      for (int sg = 0;; ++sg) {
+        const int ri = sg % NSEG;
+        if (!(ok = wait_bar1(bar(BAR_SEGF + ri), (sg / NSEG) & 1, abort_flag))) break;
+        const SegDesc& d = seg_ring[ri];
+        const int end = d.end;
+        const int j0 = d.j0, j1 = d.j1, L = d.L;
+        const int je_a = min(j1, d.nblk_a), je_b = min(j1, d.nblk_b);
+        if (end) break;
+        mbar_arrive(bar(BAR_SEGE + ri));
+        if (!(ok = wait_bar1(bar(BAR_QF + 0), sg & 1, abort_flag))) break;
+        if (!(ok = wait_bar1(bar(BAR_QF + 1), sg & 1, abort_flag))) break;
         // a tile without QK in this segment releases its Q at once
         if (je_a <= j0) mma_commit(bar(BAR_QE + 0));
         if (je_b <= j0) mma_commit(bar(BAR_QE + 1));
-      }
-      __syncwarp();
-      for (int j = j0; j <= j1 && ok; ++j) {
-        const bool has_qk = j < j1;
-        const int tt = t + (j - j0);              // global block index of block j
-        const int st = tt % NSTAGE, pst = (tt + NSTAGE - 1) % NSTAGE;
-        bool k_ready = false;                     // K(j) is waited for only before the first QK
-        if (j > j0) {
-          if (!(ok = wait_bar(bar(BAR_VF + pst), ((tt - 1) / NSTAGE) & 1, abort_flag))) break;
-          const int kbase = (j - 1) * BN;
-          if (kbase + BN > L) {
-            // zero V rows at positions >= L (both 64-channel halves of each row)
-            const int first_row = L - kbase;
-            uint8_t* vt = base + OFF_V + pst * TILE;
-            for (int idx = lane; idx < (BN - first_row) * 16; idx += 32) {
-              const int row = first_row + (idx >> 4), cc = idx & 15;
-              *reinterpret_cast<uint4*>(vt + (cc >> 3) * HALF + row * 128 + (cc & 7) * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
+        for (int j = j0; j <= j1 && ok; ++j) {
+          const bool has_qk = j < j1;
+          const int tt = t + (j - j0);              // global block index of block j
+          const int st = tt % NSTAGE, pst = (tt + NSTAGE - 1) % NSTAGE;
+          bool k_ready = false;                     // K(j) is waited for only before the first QK
+          if (j > j0) {
+            if (!(ok = wait_bar1(bar(BAR_VF + pst), ((tt - 1) / NSTAGE) & 1, abort_flag))) break;
+            const int kbase = (j - 1) * BN;
+            if (kbase + BN > L) {
+              // zero V rows at positions >= L (both 64-channel halves of each
+              // row; rare: the last block of a sequence)
+              const int first_row = L - kbase;
+              uint8_t* vt = base + OFF_V + pst * TILE;
+              for (int idx = 0; idx < (BN - first_row) * 16; ++idx) {
+                const int row = first_row + (idx >> 4), cc = idx & 15;
+                *reinterpret_cast<uint4*>(vt + (cc >> 3) * HALF + row * 128 + (cc & 7) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_async_smem();
             }
-            fence_async_smem();
-            __syncwarp();
           }
-        }
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          const int jex = x == 0 ? je_a : je_b;
-          int& cnt = x == 0 ? cnt_a : cnt_b;
-          if (j > j0 && j - 1 < jex) {
-            if (!(ok = wait_bar(bar(BAR_PF + x), cnt & 1, abort_flag))) break;
-            ++cnt;
-            tc_fence_after();
-            if (lane == 0) {
+          for (int x = 0; x < 2; ++x) {
+            const int jex = x == 0 ? je_a : je_b;
+            int& cnt = x == 0 ? cnt_a : cnt_b;
+            if (j > j0 && j - 1 < jex) {
+              if (!(ok = wait_bar1(bar(BAR_PF + x), cnt & 1, abort_flag))) break;
+              ++cnt;
+              tc_fence_after();
               const uint32_t v_s = base_s + OFF_V + pst * TILE;
               mma8_pv_ts(tmem + tm_o(x), tmem + tm_p(x), desc_mnmajor(v_s), IDESC_PV,
                          j - 1 > j0 ? 1u : 0u);
               if (j == jex) mma_commit(bar(BAR_OD + x));
             }
-            __syncwarp();
-          }
-          if (has_qk && j < jex) {
-            if (!k_ready) {
-              if (!(ok = wait_bar(bar(BAR_KF + st), (tt / NSTAGE) & 1, abort_flag))) break;
-              k_ready = true;
-            }
-            tc_fence_after();
-            if (lane == 0) {
+            if (has_qk && j < jex) {
+              if (!k_ready) {
+                if (!(ok = wait_bar1(bar(BAR_KF + st), (tt / NSTAGE) & 1, abort_flag))) break;
+                k_ready = true;
+              }
+              tc_fence_after();
               const uint32_t q_s = base_s + OFF_Q + x * TILE, k_s = base_s + OFF_K + st * TILE;
               mma8_qk(tmem + tm_s(x), desc_kmajor(q_s), desc_kmajor(k_s), IDESC_QK);
               mma_commit(bar(BAR_SF + x));
               if (j == jex - 1) mma_commit(bar(BAR_QE + x));
             }
-            __syncwarp();
           }
-        }
-        if (!ok) break;
-        if (lane == 0) {
+          if (!ok) break;
           if (k_ready) mma_commit(bar(BAR_KE + st));
           if (j > j0) mma_commit(bar(BAR_VE + pst));
         }
-        __syncwarp();
+        if (!ok) break;
+        t += j1 - j0;
       }
-      if (!ok) break;
-      t += j1 - j0;
+      // drain: every MMA issued above completes before TMEM is released
+      mma_commit(bar(BAR_DR));
+      (void)mbar_wait(bar(BAR_DR), 0);
     }
-    // drain: every MMA issued above completes before TMEM is released
-    if (lane == 0) mma_commit(bar(BAR_DR));
     __syncwarp();
-    (void)mbar_wait(bar(BAR_DR), 0);
   } else {
     // ---------------------------------------------------------- softmax
     // Per segment the block loop keeps only what it needs in registers; the
