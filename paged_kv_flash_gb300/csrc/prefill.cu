@@ -83,11 +83,12 @@ constexpr int OFF_Q = 0;                      // Q_A, Q_B
 constexpr int OFF_K = OFF_Q + 2 * TILE;
 constexpr int OFF_V = OFF_K + NSTAGE * TILE;
 constexpr int OFF_BAR = OFF_V + NSTAGE * TILE;
-// barriers (pairs are per tile or per ring stage): q_full, q_empty, k_full,
-// k_empty, v_full, v_empty, s_full, p_full, o_done, drain, seg_full,
-// seg_empty, and per tile for a cut unit: st (the tile's 4 warps have
-// stored their part), go (every other part is counted: merge)
-constexpr int BAR_QF = 0, BAR_QE = 2, BAR_KF = 4, BAR_KE = 6, BAR_VF = 8, BAR_VE = 10,
+// barriers (pairs are per tile or per ring slot): q_full, q_empty, ld (the
+// loads of one phase have landed), xe (the MMAs that read a phase's
+// buffers are done), s_full, p_full, o_done, drain, seg_full, seg_empty,
+// and per tile for a cut unit: st (the tile's 4 warps have stored their
+// part), go (every other part is counted: merge)
+constexpr int BAR_QF = 0, BAR_QE = 2, BAR_LD = 4, BAR_XE = 6,
               BAR_SF = 12, BAR_PF = 14, BAR_OD = 16, BAR_DR = 18, BAR_SEGF = 19,
               BAR_SEGE = 21, BAR_ST = 23, BAR_GO = 25, NUM_BARS = 27;
 constexpr int NSEG = 2;                       // segment descriptor ring depth
@@ -688,10 +689,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(BAR_QF + x), 1);
       mbar_init(bar(BAR_QE + x), 1);
-      mbar_init(bar(BAR_KF + x), 1);
-      mbar_init(bar(BAR_KE + x), 1);
-      mbar_init(bar(BAR_VF + x), 1);
-      mbar_init(bar(BAR_VE + x), 1);
+      mbar_init(bar(BAR_LD + x), 1);
+      mbar_init(bar(BAR_XE + x), 1);
       mbar_init(bar(BAR_SF + x), 1);
       mbar_init(bar(BAR_PF + x), BM);
       mbar_init(bar(BAR_OD + x), 1);
@@ -714,14 +713,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  static_assert(NSTAGE == 2, "the producer tracks two stages");
-  // last issued load per K/V stage and number of Q loads per tile (for the
-  // drain after an abort)
-  int last_k0 = -1, last_k1 = -1, last_v0 = -1, last_v1 = -1, nq_a = 0, nq_b = 0;
+  static_assert(NSTAGE == 2, "the producer tracks two ring slots");
+  // last armed load phase per ring slot and number of Q loads per tile (for
+  // the drain after an abort)
+  int last_ph0 = -1, last_ph1 = -1, nq_a = 0, nq_b = 0;
   if (warp == WARP_TMA) {
     // ------------------------------------------------ scheduler + producer
     bool ok = true;
-    int t = 0;                                    // K/V blocks issued so far
+    int ph = 0;                                   // load phases armed so far
     for (int sg = 0;; ++sg) {
       int j0 = 0, j1 = 0, cf = cta, nown = 1;
       if (split) {
@@ -782,52 +781,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int lp = j * (BN / kPageSize) + lane;
         return (lane < BN / kPageSize && lp < npages) ? __ldg(bt_row + lp) : 0;
       };
-      // K and V of block j (global block index t): the K boxes, then (after
-      // `between`) the V boxes.  Lane i < 8 loads page i of the block (both
-      // 64-channel halves), so a block takes four TMA instructions, and the
-      // next block's page ids are read while this block's waits run.
-      auto nothing = []() { return true; };
-      int pg_next = 0;
-      auto issue_kv = [&](int j, auto&& between) -> bool {
-        const int st = t % NSTAGE;
-        int pg = pg_next;
-        if (j + 1 < j1) pg_next = page_ids(j + 1);
-        if (pg < 0 || pg >= a.num_pages) {
-          atomicOr(&g_err_prefill, kErrBadIndex);
-          pg = 0;
+      // Load phases.  Phase j of a segment (j = j0 .. j1) carries V of block
+      // j - 1 (if j > j0) and K of block j (if j < j1), in ring slot ph % 2
+      // of both the K and the V buffers: MMA iteration j reads exactly these
+      // (PV(j - 1), then QK(j)) and frees them with one commit, so the slot
+      // is refilled for phase ph + 2 once iteration j's MMAs are done.  One
+      // barrier wait and one commit per iteration on the MMA thread, whose
+      // every barrier operation stalls the tensor core.  Lane i < 8 loads
+      // page i of a block (both 64-channel halves).
+      // lane i: page i of blocks j - 1 and j, and of block j + 1 (read one
+      // phase ahead, so that its latency overlaps this phase's wait)
+      int pg_prev = 0, pg_cur = 0, pg_next = page_ids(j0);
+      auto issue_phase = [&](int j) -> bool {
+        const bool hv = j > j0, hk = j < j1;
+        const int slot = ph & 1;
+        pg_prev = pg_cur;
+        if (hk) {
+          int pg = pg_next;
+          if (j + 1 < j1) pg_next = page_ids(j + 1);
+          if (pg < 0 || pg >= a.num_pages) {
+            atomicOr(&g_err_prefill, kErrBadIndex);
+            pg = 0;
+          }
+          pg_cur = pg;
         }
-        const int rowk = (pg * a.num_kv_heads + hkv) * kPageSize;
-        const int nload = min(BN / kPageSize, npages - j * (BN / kPageSize));
-        const uint32_t bytes = (uint32_t)nload * 2u * (kPageSize * 64 * 2);
-        if (t >= NSTAGE && !wait_bar(bar(BAR_KE + st), ((t / NSTAGE) - 1) & 1, abort_flag))
+        const int nk = hk ? min(BN / kPageSize, npages - j * (BN / kPageSize)) : 0;
+        const int nv = hv ? min(BN / kPageSize, npages - (j - 1) * (BN / kPageSize)) : 0;
+        const uint32_t bytes = (uint32_t)(nk + nv) * 2u * (kPageSize * 64 * 2);
+        if (ph >= 2 && !wait_bar(bar(BAR_XE + slot), ((ph >> 1) - 1) & 1, abort_flag))
           return false;
-        if (lane == 0) mbar_arrive_expect_tx(bar(BAR_KF + st), bytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar(BAR_LD + slot), bytes);
         __syncwarp();
-        if (lane < nload) {
-          const uint32_t dst = base_s + OFF_K + st * TILE + lane * 2048;
-          tma_load_2d(dst, &tk, 0, rowk, bar(BAR_KF + st));
-          tma_load_2d(dst + HALF, &tk, 64, rowk, bar(BAR_KF + st));
+        if (lane < nv) {
+          const int row = (pg_prev * a.num_kv_heads + hkv) * kPageSize;
+          const uint32_t dst = base_s + OFF_V + slot * TILE + lane * 2048;
+          tma_load_2d(dst, &tv, 0, row, bar(BAR_LD + slot));
+          tma_load_2d(dst + HALF, &tv, 64, row, bar(BAR_LD + slot));
         }
-        (st == 0 ? last_k0 : last_k1) = t;
-        if (!between()) return false;
-        if (t >= NSTAGE && !wait_bar(bar(BAR_VE + st), ((t / NSTAGE) - 1) & 1, abort_flag))
-          return false;
-        if (lane == 0) mbar_arrive_expect_tx(bar(BAR_VF + st), bytes);
-        __syncwarp();
-        if (lane < nload) {
-          const uint32_t dst = base_s + OFF_V + st * TILE + lane * 2048;
-          tma_load_2d(dst, &tv, 0, rowk, bar(BAR_VF + st));
-          tma_load_2d(dst + HALF, &tv, 64, rowk, bar(BAR_VF + st));
+        if (lane < nk) {
+          const int row = (pg_cur * a.num_kv_heads + hkv) * kPageSize;
+          const uint32_t dst = base_s + OFF_K + slot * TILE + lane * 2048;
+          tma_load_2d(dst, &tk, 0, row, bar(BAR_LD + slot));
+          tma_load_2d(dst + HALF, &tk, 64, row, bar(BAR_LD + slot));
         }
-        (st == 0 ? last_v0 : last_v1) = t;
-        ++t;
+        (slot == 0 ? last_ph0 : last_ph1) = ph;
+        ++ph;
         return true;
       };
       // The segment's Q tiles, each once the previous segment's last QK of
-      // that tile has completed.  They go between the first block's K (whose
-      // stage frees early) and its V (whose stage frees only when the
-      // previous segment's second-to-last PV is done), so that they land
-      // while the previous segment is still finishing.
+      // that tile has completed.  They go after the segment's first phase
+      // (K of its first block), so that they land while the previous
+      // segment is still finishing.
       auto issue_q = [&]() -> bool {
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
@@ -853,14 +857,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         return true;
       };
-      // The first segment has nothing in flight: its Q goes out first, in
-      // parallel with the page-id read for its first block.
+      // The first segment has nothing in flight: its Q goes out first.
       if (sg == 0 && !(ok = issue_q())) break;
-      pg_next = page_ids(j0);
-      auto later_q = [&]() { return sg == 0 || issue_q(); };
-      if (!(ok = issue_kv(j0, later_q))) break;
-      for (int j = j0 + 1; j < j1; ++j)
-        if (!(ok = issue_kv(j, nothing))) break;
+      if (!(ok = issue_phase(j0))) break;
+      if (sg > 0 && !(ok = issue_q())) break;
+      for (int j = j0 + 1; j <= j1; ++j)
+        if (!(ok = issue_phase(j))) break;
       if (!ok) break;
       if (split) {
         if (c.ustart <= lo) c.end = true;         // this unit opens the range: done
@@ -885,7 +887,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // lands.
     if (lane == 0) {
       bool ok = true;
-      int t = 0, cnt_a = 0, cnt_b = 0;
+      int ph = 0, cnt_a = 0, cnt_b = 0;            // load phases consumed, P tiles per tile
       for (int sg = 0;; ++sg) {
         const int ri = sg % NSEG;
         if (!(ok = wait_bar1(bar(BAR_SEGF + ri), (sg / NSEG) & 1, abort_flag))) break;
@@ -900,19 +902,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // a tile without QK in this segment releases its Q at once
         if (je_a <= j0) mma_commit(bar(BAR_QE + 0));
         if (je_b <= j0) mma_commit(bar(BAR_QE + 1));
-        for (int j = j0; j <= j1 && ok; ++j) {
+        for (int j = j0; j <= j1 && ok; ++j, ++ph) {
           const bool has_qk = j < j1;
-          const int tt = t + (j - j0);              // global block index of block j
-          const int st = tt % NSTAGE, pst = (tt + NSTAGE - 1) % NSTAGE;
-          bool k_ready = false;                     // K(j) is waited for only before the first QK
+          const int slot = ph & 1;                  // V(j - 1) and K(j) of this phase
+          if (!(ok = wait_bar1(bar(BAR_LD + slot), (ph >> 1) & 1, abort_flag))) break;
           if (j > j0) {
-            if (!(ok = wait_bar1(bar(BAR_VF + pst), ((tt - 1) / NSTAGE) & 1, abort_flag))) break;
             const int kbase = (j - 1) * BN;
             if (kbase + BN > L) {
               // zero V rows at positions >= L (both 64-channel halves of each
               // row; rare: the last block of a sequence)
               const int first_row = L - kbase;
-              uint8_t* vt = base + OFF_V + pst * TILE;
+              uint8_t* vt = base + OFF_V + slot * TILE;
               for (int idx = 0; idx < (BN - first_row) * 16; ++idx) {
                 const int row = first_row + (idx >> 4), cc = idx & 15;
                 *reinterpret_cast<uint4*>(vt + (cc >> 3) * HALF + row * 128 + (cc & 7) * 16) =
@@ -929,29 +929,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (!(ok = wait_bar1(bar(BAR_PF + x), cnt & 1, abort_flag))) break;
               ++cnt;
               tc_fence_after();
-              const uint32_t v_s = base_s + OFF_V + pst * TILE;
+              const uint32_t v_s = base_s + OFF_V + slot * TILE;
               mma8_pv_ts(tmem + tm_o(x), tmem + tm_p(x), desc_mnmajor(v_s), IDESC_PV,
                          j - 1 > j0 ? 1u : 0u);
               if (j == jex) mma_commit(bar(BAR_OD + x));
             }
             if (has_qk && j < jex) {
-              if (!k_ready) {
-                if (!(ok = wait_bar1(bar(BAR_KF + st), (tt / NSTAGE) & 1, abort_flag))) break;
-                k_ready = true;
-              }
               tc_fence_after();
-              const uint32_t q_s = base_s + OFF_Q + x * TILE, k_s = base_s + OFF_K + st * TILE;
+              const uint32_t q_s = base_s + OFF_Q + x * TILE, k_s = base_s + OFF_K + slot * TILE;
               mma8_qk(tmem + tm_s(x), desc_kmajor(q_s), desc_kmajor(k_s), IDESC_QK);
               mma_commit(bar(BAR_SF + x));
               if (j == jex - 1) mma_commit(bar(BAR_QE + x));
             }
           }
           if (!ok) break;
-          if (k_ready) mma_commit(bar(BAR_KE + st));
-          if (j > j0) mma_commit(bar(BAR_VE + pst));
+          mma_commit(bar(BAR_XE + slot));           // this phase's K and V are read
         }
         if (!ok) break;
-        t += j1 - j0;
       }
       // drain: every MMA issued above completes before TMEM is released
       mma_commit(bar(BAR_DR));
@@ -1218,10 +1212,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // flight: the producer lets each one land before the CTA can exit.
   __syncthreads();
   if (warp == WARP_TMA && *abort_flag) {
-    if (last_k0 >= 0) (void)mbar_wait(bar(BAR_KF + 0), (last_k0 / NSTAGE) & 1);
-    if (last_k1 >= 0) (void)mbar_wait(bar(BAR_KF + 1), (last_k1 / NSTAGE) & 1);
-    if (last_v0 >= 0) (void)mbar_wait(bar(BAR_VF + 0), (last_v0 / NSTAGE) & 1);
-    if (last_v1 >= 0) (void)mbar_wait(bar(BAR_VF + 1), (last_v1 / NSTAGE) & 1);
+    if (last_ph0 >= 0) (void)mbar_wait(bar(BAR_LD + 0), (last_ph0 >> 1) & 1);
+    if (last_ph1 >= 0) (void)mbar_wait(bar(BAR_LD + 1), (last_ph1 >> 1) & 1);
     if (nq_a > 0) (void)mbar_wait(bar(BAR_QF + 0), (nq_a - 1) & 1);
     if (nq_b > 0) (void)mbar_wait(bar(BAR_QF + 1), (nq_b - 1) & 1);
   }
