@@ -706,12 +706,81 @@ def cpu_baseline(mixed_wl, budget_s=20.0):
 
 # ------------------------------------------------------- profiling cases
 
+def _decode_fn(torch, pk, case, pool, smooth=None):
+    q = to_dev_bf16(torch, case.q)
+    bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
+    ms = int(case.seq_lens.max())
+    _, _, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
+    ws = pk.decode_workspace(wsb, zb)
+    out = torch.empty_like(q)
+    lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
+    w = to_dev(torch, smooth) if smooth is not None else None
+    return lambda: pk.paged_attn_decode(pool, q, bt, sl, ms, SCALE, k_smooth=w, workspace=ws,
+                                        out=out, lse=lse)
+
+
+def profile_config_case(torch, pk, name):
+    """The benchmarked workloads, one kernel each, exactly as `configs` times
+    them: (launch function, algorithmic work, unit) or None for other names."""
+    if name == "decode_1k":                        # single sequence, 1,024 positions, 16/8
+        c = W.decode_1k()
+        pool = pk.Pool(to_dev_bf16(torch, c.k_pool), to_dev_bf16(torch, c.v_pool))
+        return _decode_fn(torch, pk, c, pool), decode_bytes(c.seq_lens, c.Hkv), "GB/s"
+    if name == "decode_b64":                       # 64 sequences, 512..8,192 positions, 32/8
+        c = W.batched_decode()
+        pool = pk.Pool(to_dev_bf16(torch, c.k_pool), to_dev_bf16(torch, c.v_pool))
+        return _decode_fn(torch, pk, c, pool), decode_bytes(c.seq_lens, c.Hkv), "GB/s"
+    if name in ("decode_int8_b1", "decode_int8_b8", "append_int8_32k"):
+        B = 8 if name == "decode_int8_b8" else 1
+        app, qh = W.int8_long_decode(B=B)
+        pool = pk.Pool.empty(app.layout.num_pages, app.Hkv, dtype=torch.int8)
+        w = to_dev(torch, app.k_smooth)
+        kn, vn = to_dev_bf16(torch, app.k_new), to_dev_bf16(torch, app.v_new)
+        cu, bt, sl = (to_dev(torch, app.cu_new), to_dev(torch, app.layout.block_table),
+                      to_dev(torch, app.seq_lens))
+        ap = lambda: pk.kv_append(pool, kn, vn, cu, bt, sl, k_smooth=w)
+        ap()
+        if name == "append_int8_32k":
+            T = int(app.seq_lens.sum())
+            # bf16 K and V read, int8 codes and fp32 scales written
+            return ap, float(T * app.Hkv * (2 * 256 + 2 * (128 + 4))), "GB/s"
+        case = W.DecodeCase(32, app.Hkv, app.seq_lens, app.layout, qh, None, None)
+        return (_decode_fn(torch, pk, case, pool, app.k_smooth),
+                decode_bytes(case.seq_lens, case.Hkv, 264), "GB/s")
+    if name in ("prefill_1k", "append_bf16_1k"):   # the 1,024-token prompt, 32/8
+        app, q = W.prefill_prompt()
+        pool = pk.Pool.empty(app.layout.num_pages, app.Hkv)
+        bt, sl, cu = (to_dev(torch, app.layout.block_table), to_dev(torch, app.seq_lens),
+                      to_dev(torch, app.cu_new))
+        kn, vn = to_dev_bf16(torch, app.k_new), to_dev_bf16(torch, app.v_new)
+        ap = lambda: pk.kv_append(pool, kn, vn, cu, bt, sl)
+        ap()
+        if name == "append_bf16_1k":
+            return ap, float(2 * 2 * 1024 * 8 * 256), "GB/s"
+        qd = to_dev_bf16(torch, q)
+        out = torch.empty_like(qd)
+        lse = torch.empty((1024, 32), dtype=torch.float32, device="cuda")
+        ws_p = pk.prefill_workspace()
+        return (lambda: pk.paged_attn_prefill(pool, qd, cu, bt, sl, 1024, SCALE, workspace=ws_p,
+                                              out=out, lse=lse),
+                prefill_flops(1024, 1024, 32), "TFLOP/s")
+    return None
+
+
+PROFILE_CASES = ["prefill_chunk", "decode_bf16", "decode_int8", "qkv_prep", "verify_step",
+                 "decode_1k", "decode_b64", "decode_int8_b1", "decode_int8_b8",
+                 "append_int8_32k", "prefill_1k", "append_bf16_1k"]
+
+
 def profile_case(torch, pk, name, reps=3):
     """One kernel on a fixed, seeded workload, launched `reps` times (for ncu
     captures of a single launch: -k <kernel> -s 2 -c 1).  Prints the median
     CUDA-event time of 10 more launches, each after an L2 flush."""
     rng = np.random.default_rng(5)
-    if name == "prefill_chunk":
+    cfg = profile_config_case(torch, pk, name)
+    if cfg is not None:
+        fn, work, unit = cfg
+    elif name == "prefill_chunk":
         qlen, L = 2048, 16384
         case = W.decode_bf16(rng, [L], 32, 8)
         q = to_dev_bf16(torch, W.normal_bf16(rng, (qlen, 32, D)))
@@ -876,8 +945,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["prefill_chunk", "decode_bf16", "decode_int8",
-                                                      "qkv_prep", "verify_step"],
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
                     help="run one kernel on a fixed workload (for ncu) and exit")
     args = ap.parse_args(argv)
     K, Wu = args.steps, max(3, args.warmup)
