@@ -651,16 +651,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   Cursor c;
   c.end = true;
   if (warp == WARP_TMA) {
-    // the first block's page ids of the first sequence: usually needed first
-    if (lane < BN / kPageSize && lane < a.max_pages)
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + lane));
-    // whole units' makespan vs the split share (in double: the products of
-    // large launches would not fit 64 bits, and this is only an estimate)
+    // the first sequence's block-table row (a CTA's first block may lie
+    // anywhere in it), fetched into L2 while the walk is planned
+    for (int e = lane * 32; e < a.max_pages; e += 32 * 32)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a.block_table + e));
+    // whole units' makespan vs the split share (in fp32: the products of
+    // large launches would not fit 64 bits, and this is only an estimate;
+    // fp64 is slow on this GPU)
     auto cut = [&](long long w, int um, long long n) {
       if (n <= 0) return false;
-      const double per = (double)((n + P - 1) / P);
-      const double whole = fmax((double)um, per * (double)w / (double)n);
-      return whole > (double)w / (double)P + (double)kSplitGain;
+      const float per = (float)((n + P - 1) / P);
+      const float whole = fmaxf((float)um, per * (float)w / (float)n);
+      return whole > (float)w / (float)P + (float)kSplitGain;
     };
     int umax = 0;
     long long units = 0;
