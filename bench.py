@@ -1000,7 +1000,10 @@ def main(argv=None):
                                             f"{spent:.1f} s; scaled by (row, head, key) "
                                             f"triples to the full step")},
                 "e2e": {"value": round(v, 1), "unit": "us", "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
+                        "d2h_bytes_per_step": 0},
+                "sampled_cpu_seconds": round(spent, 2),
+                "value_note": ("per-step time of the whole step extrapolated from the sampled "
+                               "rows; the run itself spent sampled_cpu_seconds")}
         print(json.dumps(line), flush=True)
         return 0
 
