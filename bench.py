@@ -7,16 +7,21 @@ One bench step is one continuous-batching step of the mixed workload (a
 Llama-3.1-8B-like layer, GQA 32/8, head_dim 128, 16-token pages): one
 26,926-token prompt prefilled in 2,048-row chunks against its own cached
 prefix, plus 32 decode rows with contexts ~ U[128, 16384]; step c appends
-chunk c and one token per decode row (kv_append), prefills chunk c
-(paged_attn_prefill), then decodes the 32 rows (paged_attn_decode: split
-kernel + combine).  Steps cycle through the 14 chunks; with K a multiple of
+chunk c and one token per decode row (kv_append), then prefills chunk c
+(paged_attn_prefill) and decodes the 32 rows (paged_attn_decode: split
+kernel + combine).  Both need only the append, so they run side by side:
+the prefill, bound by the tensor cores, on part of the SMs
+(pkv_overlap_prefill_ctas) and the decode, bound by HBM, on a second stream
+over the rest (--sequential runs them one after the other on one stream).
+Steps cycle through the 14 chunks; with K a multiple of
 14 every chunk is timed equally often.  All inputs (1.2 GB pool, every
 step's rows) are resident in HBM before the timed region; the pool is larger
 than L2, so no separate flush is needed there.
 
 The JSON line reports the step time (value, us per step) and, from CUDA
-events around every call, decode HBM GB/s and prefill TFLOP/s; the roofline
-object is for the prefill kernel, which dominates the step.  "configs" holds
+events around every call (on the stream that runs it), decode HBM GB/s and
+prefill TFLOP/s; the roofline object is for the prefill kernel, which
+dominates the step, with the share of the SMs it held.  "configs" holds
 the other workloads (single-sequence decode, 1,024-token prefill, batched
 decode, INT8 32k decode, 16-token verify steps through the multi-token
 decode, the fused attention-input step on a 2,048-token chunk) timed with a
@@ -185,10 +190,17 @@ def decode_bytes(lens, Hkv, per_pos=2 * D * 2):
 # ------------------------------------------------------- mixed workload
 
 class Mixed:
-    """Device-resident mixed workload and its step function."""
+    """Device-resident mixed workload and its step function.  overlap: the
+    prefill runs on part of the SMs (pkv_overlap_prefill_ctas) while the
+    decode runs beside it on a second stream; else one after the other."""
 
-    def __init__(self, torch, pk):
+    def __init__(self, torch, pk, overlap=True):
         self.torch, self.pk = torch, pk
+        self.overlap = overlap
+        # the prefill's stream goes first when both wait for the append, so
+        # that it takes its SMs and the decode's CTAs fill the others
+        self.s_pre = torch.cuda.Stream(priority=-1)
+        self.s_dec = torch.cuda.Stream()
         wl = W.mixed_step()
         self.wl = wl
         self.R = len(wl.decode_lens0)
@@ -213,6 +225,7 @@ class Mixed:
                 host=s)
             S, C, ws, _ = pk.decode_plan(self.R, wl.Hq, wl.Hkv, st["max_dec"])
             st["splits"] = S
+            st["ctas"] = pk.overlap_prefill_ctas(st["flops"], st["dbytes"])
             st["launches"] = 3 + (1 if S > 1 else 0)
             self.steps.append(st)
         plans = [pk.decode_plan(self.R, wl.Hq, wl.Hkv, s["max_dec"]) for s in self.steps]
@@ -225,24 +238,38 @@ class Mixed:
         self.lse_d = torch.empty((self.R, wl.Hq), dtype=torch.float32, device="cuda")
 
     def step(self, i, ev=None, inputs=None, outs=None):
-        """Step i (chunk i mod 14).  ev: list of 3 event pairs to record
-        (append, prefill, decode) or None.  inputs: per-step device tensors
+        """Step i (chunk i mod 14) on the current stream's timeline: it starts
+        after the work queued there and the work queued there after it waits
+        for it.  ev: 5 events to record (step start, append end, prefill end,
+        decode start, decode end) or None.  inputs: per-step device tensors
         that replace the resident ones (end-to-end path); outs: (out_p,
         lse_p, out_d, lse_d) to write instead of the resident outputs."""
-        pk, wl = self.pk, self.wl
+        torch, pk, wl = self.torch, self.pk, self.wl
         st = self.steps[i % len(self.steps)]
         x = inputs or st
         out_p, lse_p, out_d, lse_d = outs or (self.out_p, self.lse_p, self.out_d, self.lse_d)
         n = st["chunk_len"]
-        if ev: ev[0].record()
-        pk.kv_append(self.pool, x["k_new"], x["v_new"], st["cu_app"], self.bt_all, st["lens_app"])
-        if ev: ev[1].record()
+        cur = torch.cuda.current_stream()
+        sp = self.s_pre if self.overlap else cur
+        sd = self.s_dec if self.overlap else cur
+        sp.wait_stream(cur)
+        if ev: ev[0].record(sp)
+        pk.kv_append(self.pool, x["k_new"], x["v_new"], st["cu_app"], self.bt_all, st["lens_app"],
+                     stream=sp)
+        if ev: ev[1].record(sp)
+        if self.overlap:
+            sd.wait_stream(sp)                    # the decode needs the append only
         pk.paged_attn_prefill(self.pool, x["q_chunk"], st["cu_q"], self.bt_prompt, st["lens_p"],
-                              n, SCALE, workspace=self.ws_p, out=out_p[:n], lse=lse_p[:n])
-        if ev: ev[2].record()
+                              n, SCALE, workspace=self.ws_p, out=out_p[:n], lse=lse_p[:n],
+                              stream=sp, num_ctas=st["ctas"] if self.overlap else 0)
+        if ev: ev[2].record(sp)
+        if ev: ev[3].record(sd)
         pk.paged_attn_decode(self.pool, x["q_dec"], self.bt_dec, st["lens_d"], st["max_dec"],
-                             SCALE, workspace=self.ws, out=out_d, lse=lse_d)
-        if ev: ev[3].record()
+                             SCALE, workspace=self.ws, out=out_d, lse=lse_d, stream=sd)
+        if ev: ev[4].record(sd)
+        if self.overlap:
+            cur.wait_stream(sp)
+            cur.wait_stream(sd)
 
 
 def max_over_ranks(torch, x):
@@ -264,8 +291,8 @@ def time_mixed(torch, pk, mixed, K, Wu, world, rank):
     torch.cuda.synchronize()
     assert pk.poll_device_error() == pk.OK, "device-side error during warm-up"
     nsteps = len(mixed.steps)
-    # per-step events (append / prefill / decode boundaries)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # per-step events (step start, append end, prefill end, decode start and end)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
@@ -289,15 +316,19 @@ def time_mixed(torch, pk, mixed, K, Wu, world, rank):
     # times, summed step times (from this step's first event to the next
     # step's), count
     per = [[0.0, 0.0, 0.0, 0.0, 0] for _ in range(nsteps)]
+    cta_ms = 0.0                                  # prefill time x its CTA count
+    all_ctas = pk.prefill_plan()[0]
+    ctas_of = lambda st: st["ctas"] if mixed.overlap else all_ctas
     for i in range(K):
         e = evs[i]
         c = (Wu + i) % nsteps
         st = mixed.steps[c]
-        a, p, d = e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])
+        a, p, d = e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[3].elapsed_time(e[4])
         whole = e[0].elapsed_time(evs[i + 1][0] if i + 1 < K else t1)
         app_ms += a
         pre_ms += p
         dec_ms += d
+        cta_ms += p * ctas_of(st)
         for j, v in enumerate((a, p, d, whole)):
             per[c][j] += v
         per[c][4] += 1
@@ -310,6 +341,7 @@ def time_mixed(torch, pk, mixed, K, Wu, world, rank):
             continue
         st = mixed.steps[c]
         chunks.append({"chunk": c, "rows": st["chunk_len"], "context": st["context"],
+                       "prefill_ctas": ctas_of(st),
                        "step_us": round(w * 1e3 / n, 2),
                        "append_us": round(a * 1e3 / n, 2), "prefill_us": round(p * 1e3 / n, 2),
                        "prefill_TFLOPs": round(st["flops"] / (p * 1e-3 / n) / 1e12, 1),
@@ -327,7 +359,8 @@ def time_mixed(torch, pk, mixed, K, Wu, world, rank):
     total_ms = max_over_ranks(torch, total_ms)
     return dict(total_ms=total_ms, step_ms=step_ms, balanced=balanced, app_ms=app_ms,
                 pre_ms=pre_ms, dec_ms=dec_ms, flops=flops, dbytes=dbytes, launches=launches,
-                clocks=clk, chunks=chunks)
+                clocks=clk, chunks=chunks, overlap=mixed.overlap, steps=K,
+                sm_share=cta_ms / pre_ms / all_ctas if pre_ms > 0 else 1.0)
 
 
 def time_e2e(torch, pk, mixed, K, first):
@@ -457,7 +490,7 @@ def other_configs(torch, pk, hbm, bf16):
         q = to_dev_bf16(torch, case.q)
         bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
         ms = int(case.seq_lens.max())
-        S, C, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
+        S, C, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms, dtype=pool.dtype)
         ws = pk.decode_workspace(wsb, zb)
         out = torch.empty_like(q)
         lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
@@ -710,7 +743,7 @@ def _decode_fn(torch, pk, case, pool, smooth=None):
     q = to_dev_bf16(torch, case.q)
     bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
     ms = int(case.seq_lens.max())
-    _, _, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
+    _, _, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms, dtype=pool.dtype)
     ws = pk.decode_workspace(wsb, zb)
     out = torch.empty_like(q)
     lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
@@ -811,7 +844,7 @@ def profile_case(torch, pk, name, reps=3):
         q = to_dev_bf16(torch, case.q)
         bt, sl = to_dev(torch, case.layout.block_table), to_dev(torch, case.seq_lens)
         ms = int(case.seq_lens.max())
-        _, _, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms)
+        _, _, wsb, zb = pk.decode_plan(case.B, case.Hq, case.Hkv, ms, dtype=pool.dtype)
         ws = pk.decode_workspace(wsb, zb)
         out = torch.empty_like(q)
         lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
@@ -890,6 +923,22 @@ def make_line(K, Wu, world, r, e2e, peaks_, prof, config, nsteps=14):
         roofline["clock_note"] = (f"peak scaled by bench SM clock {sm_mhz:.0f} MHz / "
                                   f"{peak_mhz:.0f} MHz median under load when the peaks were "
                                   "measured")
+    share = r.get("sm_share", 1.0)
+    alone = r.get("alone")
+    if alone:
+        a_tf = alone["flops"] / (alone["pre_ms"] * 1e-3) / 1e12
+        roofline["achieved_alone"] = round(a_tf, 1)
+        roofline["frac_alone"] = round(a_tf / peak, 4)
+        roofline["alone_note"] = ("the same steps run one after the other right after the timed "
+                                  f"region ({alone['steps']} steps): the prefill alone on every SM")
+    if r.get("overlap"):
+        # the prefill held part of the SMs (the decode ran beside it on the
+        # others): its attainable peak is that share of the GPU's
+        roofline["sm_share"] = round(share, 4)
+        roofline["frac_of_sm_share"] = round(frac / share, 4)
+        roofline["sm_share_note"] = ("prefill launches ran on part of the SMs (time-weighted "
+                                     "mean CTAs / all) beside the decode on a second stream; "
+                                     "frac_of_sm_share = achieved / (peak x sm_share)")
     if "tensor_pipe_active_pct_2048x16384" in prof:
         roofline["ncu_tensor_pipe_active_pct"] = prof["tensor_pipe_active_pct_2048x16384"]
         roofline["ncu_note"] = ("sm__pipe_tensor_cycles_active of one 2,048-row x 16,384-"
@@ -904,6 +953,9 @@ def make_line(K, Wu, world, r, e2e, peaks_, prof, config, nsteps=14):
                        "each chunk's mean step time)" if r["balanced"] else
                        "us per step, plain mean (fewer than 14 steps timed)"),
         "plain_mean_us": round(r["total_ms"] * 1e3 / K, 2),
+        "schedule": ("overlapped: append, then the prefill on part of the SMs "
+                     "(pkv_overlap_prefill_ctas) beside the decode on a second stream"
+                     if r.get("overlap") else "sequential: append, prefill, decode on one stream"),
         "decode": {"us_per_step": round(r["dec_ms"] * 1e3 / K, 2), "GBps": round(dec_gbs, 1),
                    "frac_of_8TBps": round(dec_gbs / NOMINAL_HBM_GBS, 4),
                    "frac_of_measured": round(dec_gbs / hbm, 4),
@@ -932,6 +984,27 @@ def make_line(K, Wu, world, r, e2e, peaks_, prof, config, nsteps=14):
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if alone:
+        a_dec = alone["dbytes"] / (alone["dec_ms"] * 1e-3) / 1e9
+        a_pre = alone["flops"] / (alone["pre_ms"] * 1e-3) / 1e12
+        n_a = alone["steps"]
+        line["sequential"] = {
+            "note": ("the same steps one after the other on one stream (each kernel alone on "
+                     "the GPU), timed right after the overlapped region"),
+            "steps": n_a, "value": round(alone["step_ms"] * 1e3, 2),
+            "decode": {"us_per_step": round(alone["dec_ms"] * 1e3 / n_a, 2),
+                       "GBps": round(a_dec, 1), "frac_of_measured": round(a_dec / hbm, 4),
+                       "frac_of_8TBps": round(a_dec / NOMINAL_HBM_GBS, 4)},
+            "prefill": {"us_per_step": round(alone["pre_ms"] * 1e3 / n_a, 2),
+                        "TFLOPs": round(a_pre, 1),
+                        "frac_of_measured_burst": round(a_pre / bf16, 4),
+                        "frac_of_spec_dense": round(a_pre / SPEC_BF16_TFLOPS, 4)},
+            "append": {"us_per_step": round(alone["app_ms"] * 1e3 / n_a, 2)}}
+        line["decode"]["note"] = ("overlapped with the prefill: time from the decode's start to "
+                                  "its end while the prefill holds most SMs (alone: see "
+                                  "'sequential')")
+        line["prefill"]["note"] = ("overlapped with the decode, on part of the SMs (see "
+                                   "roofline.sm_share; alone: see 'sequential')")
     return line
 
 
@@ -945,6 +1018,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sequential", action="store_true",
+                    help="mixed step on one stream (no prefill/decode overlap)")
     ap.add_argument("--profile-case", choices=PROFILE_CASES,
                     help="run one kernel on a fixed workload (for ncu) and exit")
     args = ap.parse_args(argv)
@@ -956,7 +1031,9 @@ def main(argv=None):
 
     config = {"workload": ("mixed continuous-batching step: one 26,926-token causal prompt "
                            "prefilled in 2,048-row chunks against its cached prefix + 32 decode "
-                           "rows (contexts U[128,16384]); append -> prefill -> decode per step"),
+                           "rows (contexts U[128,16384]); per step the append, then the prefill "
+                           "and the decode (both after the append; overlapped on two streams "
+                           "unless --sequential)"),
               "heads_q": 32, "heads_kv": 8, "head_dim": 128, "page_size": 16,
               "prompt_len": 26926, "chunk": 2048, "decode_rows": 32,
               "l2": "working set 1.2 GB > 129 MB L2 (no flush between steps)",
@@ -1020,9 +1097,15 @@ def main(argv=None):
         profile_case(torch, pk, args.profile_case)
         return 0
     hbm, bf16, bf16_sus, peak_src, peak_mhz = peaks()
-    mixed = Mixed(torch, pk)
+    mixed = Mixed(torch, pk, overlap=not args.sequential)
     r = time_mixed(torch, pk, mixed, K, Wu, world, rank)
     nsteps = len(mixed.steps)
+    if mixed.overlap:
+        # the same steps one after the other, briefly: each kernel alone on
+        # the whole GPU, for the per-kernel figures beside the overlapped step
+        mixed.overlap = False
+        r["alone"] = time_mixed(torch, pk, mixed, 20 * nsteps, nsteps, world, rank)
+        mixed.overlap = True
     K_e2e = -(-K // nsteps) * nsteps               # whole passes over the 14 chunks
     e2e_us, h2d, d2h = time_e2e(torch, pk, mixed, K_e2e, Wu)
 

@@ -102,8 +102,11 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
 /*
  * Split plan of a decode call ("Fused kernels ...": split-KV for decode).
  * Host-only; launches nothing.  max_seq_len (host) bounds every seq_lens[b];
- * num_splits 0 asks for the built-in heuristic (split count chosen from the
- * batch, the heads and the device's SM count), > 0 forces that many splits.
+ * dtype is the pool's pkv_kv_dtype (the heuristic gives INT8 pages, half the
+ * bytes, longer splits; a bf16 plan's workspace is never smaller than the
+ * INT8 plan's of the same shape); num_splits 0 asks for the built-in
+ * heuristic (split count chosen from the batch, the heads, the dtype and the
+ * device's SM count), > 0 forces that many splits.
  * Outputs (host pointers, each may be NULL): the split count S, the pages per
  * split, the workspace bytes the decode call needs (0 when S == 1), and how
  * many leading bytes of that workspace must be zero before its first use
@@ -112,7 +115,8 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
  * num_splits > 1 for them is PKV_ERR_INVALID.
  */
 pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                           int32_t max_seq_len, int32_t num_splits, int32_t* splits_out,
+                           int32_t max_seq_len, int32_t dtype, int32_t num_splits,
+                           int32_t* splits_out,
                            int32_t* pages_per_split_out, size_t* workspace_bytes_out,
                            size_t* zero_bytes_out);
 
@@ -129,7 +133,8 @@ pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_he
  *  k_smooth     INT8 pools: the same fp32 [128] weight given to kv_append,
  *               or NULL if the keys were not smoothed; NULL for bf16.
  *  num_splits   0 = heuristic, > 0 forces (see pkv_decode_plan).
- *  workspace    scratch of at least pkv_decode_plan's bytes (256-byte
+ *  workspace    scratch of at least pkv_decode_plan's bytes for this pool's
+ *               dtype and these sizes (256-byte
  *               aligned), may be NULL when that is 0.  Holds the split
  *               partials; its contents are dead after the call (its first
  *               zero_bytes are not used by this call).
@@ -247,6 +252,13 @@ pkv_status pkv_prefill_plan(int32_t* ctas, size_t* workspace_bytes, size_t* zero
  *            last blocks merges them (the log-sum-exp rule of "Split-KV
  *            decoding").  PKV_ERR_INVALID if NULL, unaligned or too small.
  *            Calls that share a workspace must not overlap.
+ *  num_ctas  persistent CTAs (at most one per SM): 0 = pkv_prefill_plan's
+ *            count, every SM; 1 .. that count leaves the other SMs to work
+ *            queued on other streams -- a decode step that needs no output
+ *            of this call, for one (pkv_overlap_prefill_ctas); larger counts
+ *            run as 0.  The workspace is laid out for every SM whatever the
+ *            count, so calls with different counts share it.  Negative:
+ *            PKV_ERR_INVALID.
  *  out       bf16 [total_q][num_q_heads][128]; lse fp32 [total_q][num_q_heads]
  *            or NULL.
  * bf16 pools only (PKV_ERR_UNSUPPORTED for INT8).
@@ -257,7 +269,25 @@ pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, int32_t t
                                   const int32_t* block_table, int32_t max_pages,
                                   const int32_t* seq_lens, int32_t max_q_len,
                                   float softmax_scale, void* workspace, size_t workspace_bytes,
-                                  void* out, float* lse, void* stream);
+                                  int32_t num_ctas, void* out, float* lse, void* stream);
+
+/*
+ * overlap_prefill_ctas -- the num_ctas to give a prefill call that runs on
+ * one stream while a decode call runs on another, both after the same
+ * append (continuous batching: the prompt chunk and the decode rows of one
+ * step).  The prefill is bound by the tensor cores and scales with its SMs;
+ * the decode is bound by HBM and needs few SMs to draw most of it, so the
+ * two together finish sooner than one after the other.  prefill_flops: the
+ * prefill's causal flops (4 * 128 * num_q_heads * keys seen, summed over its
+ * rows); decode_bytes: the K/V bytes the decode reads.  The split makes the
+ * two finish together by rates measured on GB300: 1.45 PFLOP/s plus 10 us
+ * for the prefill alone, 6.5 TB/s for the decode alone, and on few SMs the
+ * decode drawing twice its whole-GPU bandwidth per SM; *ctas is in
+ * [pkv_prefill_plan's count / 3, that count].  Host only, no
+ * GPU work.  PKV_ERR_INVALID for a NULL ctas or a negative or non-finite
+ * argument.
+ */
+pkv_status pkv_overlap_prefill_ctas(double prefill_flops, double decode_bytes, int32_t* ctas);
 
 /*
  * decode_multi_plan -- split plan and workspace size of a multi-token decode

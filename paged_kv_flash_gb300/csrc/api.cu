@@ -81,13 +81,15 @@ pkv_status check_pool(const pkv_pool* pool) {
 // two CTAs resident per SM.  A CTA pays a few microseconds of start-up
 // (query and block-table loads, the first page copies), so splits are made
 // as long as the machine allows: about 0.8 CTAs per resident slot, estimated
-// from the longest sequence, with 8 to 128 pages (128 to 2,048 positions) per
-// split, a multiple of the 4 warps so that they get equal work.  Measured on
-// GB300: 64 sequences of 512..8,192 positions run best at 64..128 pages per
-// split; one 32k-position INT8 sequence at 64; eight of them at 128.  A
+// from the longest sequence, with 8 to 96 bf16 pages or 8 to 128 INT8 pages
+// (half the bytes) per split, a multiple of the 4 warps so that they get
+// equal work.  Measured on GB300: 64 sequences of 512..8,192 positions and
+// the 32 decode rows of the mixed step (contexts up to 16,384) run best at
+// 64..96 bf16 pages per split, 8 bf16 sequences of 32,768 positions at 64..96;
+// one 32k-position INT8 sequence at 64 INT8 pages, eight of them at 128.  A
 // forced split count S gives C = ceil(pages / S).
 constexpr long long kPlanSlotsNum = 4, kPlanSlotsDen = 5;   // 0.8 CTAs per slot
-constexpr long long kPlanMinPages = 8, kPlanMaxPages = 128;
+constexpr long long kPlanMinPages = 8, kPlanMaxPages = 128, kPlanMaxPagesBf16 = 96;
 
 // Workspace (splits > 1): part counters u32 [kDecodeCounters] indexed by
 // b * Hkv + h (a fixed region, so that a workspace reused by calls of any
@@ -101,7 +103,10 @@ struct Plan {
   size_t ws_bytes, ws_zero_bytes, ws_o_offset, ws_lse_offset;
 };
 
-Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, int num_splits) {
+// int8: the pool's dtype (longer splits).  The bf16 plan never has fewer
+// splits than the INT8 one, so its workspace covers both.
+Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, int num_splits,
+               bool int8) {
   const int mp = std::max(1, (max_seq_len + pkv::kPageSize - 1) / pkv::kPageSize);
   int C;
   if (num_splits > 0) {
@@ -111,7 +116,8 @@ Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, in
     const long long page_heads = (long long)batch * num_kv_heads * mp;
     const long long target = std::max<long long>(1, slots * kPlanSlotsNum / kPlanSlotsDen);
     long long c = (page_heads + target - 1) / target;
-    c = std::max<long long>(kPlanMinPages, std::min<long long>(kPlanMaxPages, c));
+    c = std::max<long long>(kPlanMinPages,
+                            std::min<long long>(int8 ? kPlanMaxPages : kPlanMaxPagesBf16, c));
     c = (c + pkv_host::kDecodeWarps - 1) / pkv_host::kDecodeWarps * pkv_host::kDecodeWarps;
     C = (int)std::min<long long>(c, mp);
   }
@@ -231,14 +237,15 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
 }
 
 pkv_status pkv_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
-                           int32_t max_seq_len, int32_t num_splits, int32_t* splits_out,
-                           int32_t* pages_per_split_out, size_t* workspace_bytes_out,
-                           size_t* zero_bytes_out) {
+                           int32_t max_seq_len, int32_t dtype, int32_t num_splits,
+                           int32_t* splits_out, int32_t* pages_per_split_out,
+                           size_t* workspace_bytes_out, size_t* zero_bytes_out) {
   if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
-      max_seq_len < 0 || num_splits < 0)
+      max_seq_len < 0 || num_splits < 0 || (dtype != PKV_BF16 && dtype != PKV_INT8))
     return PKV_ERR_INVALID;
   if (num_splits > 1 && (long long)batch * num_kv_heads > kDecodeCounters) return PKV_ERR_INVALID;
-  const Plan p = make_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits);
+  const Plan p = make_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits,
+                           dtype == PKV_INT8);
   if (splits_out) *splits_out = p.splits;
   if (pages_per_split_out) *pages_per_split_out = p.pages_per_split;
   if (workspace_bytes_out) *workspace_bytes_out = p.ws_bytes;
@@ -265,7 +272,8 @@ static pkv_status decode_call(const pkv_pool* pool, const void* q, int32_t batch
   if (pool->dtype == PKV_BF16 && k_smooth) return PKV_ERR_INVALID;
   if (num_splits > 1 && (long long)batch * pool->num_kv_heads > kDecodeCounters)
     return PKV_ERR_INVALID;
-  const Plan p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, num_splits);
+  const Plan p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, num_splits,
+                           pool->dtype == PKV_INT8);
   if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned(workspace, 256)))
     return PKV_ERR_INVALID;
   if ((long long)batch > 65535 || p.splits > 2147483647 / 2) return PKV_ERR_UNSUPPORTED;
@@ -338,13 +346,14 @@ pkv_status pkv_paged_attn_decode_noalloc(const pkv_pool* pool, const void* q, in
   if (num_splits > 1 && (long long)batch * pool->num_kv_heads > kDecodeCounters)
     return PKV_ERR_INVALID;
   const size_t cap = pkv_host::decode_fixed_scratch_bytes();
-  Plan p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, num_splits);
+  const bool int8 = pool->dtype == PKV_INT8;
+  Plan p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, num_splits, int8);
   if (p.ws_bytes > cap) {
     if (num_splits > 0) return PKV_ERR_INVALID;       // forced split count does not fit
     int s = p.splits;
     while (s > 1 && p.ws_bytes > cap) {
       --s;
-      p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, s);
+      p = make_plan(batch, num_q_heads, pool->num_kv_heads, max_seq_len, s, int8);
     }
     if (p.ws_bytes > cap) return PKV_ERR_INVALID;
   }
@@ -384,30 +393,55 @@ pkv_status pkv_prefill_plan(int32_t* ctas, size_t* workspace_bytes, size_t* zero
   return PKV_OK;
 }
 
+// Overlap of a prefill with a decode on another stream: the prefill's time
+// scales with its SMs; the decode, HBM-bound on the whole GPU, draws about
+// twice the average per-SM bandwidth when it has few SMs (measured on GB300:
+// ~85 GB/s per SM against 6.5 TB/s / 152).  Both finish together when the
+// decode holds N_d SMs with N_d / (SMs - N_d) = t_d / (kOverlapDecodeGain *
+// t_p), t_p and t_d the two calls' times alone on the whole GPU.  On the
+// mixed step (a 26,926-token prompt in 2,048-row chunks beside 32 decode
+// rows) this picks within a few percent of the best of a sweep per chunk.
+constexpr double kOverlapPrefillFlopsPerSec = 1.45e15, kOverlapPrefillFixedSec = 10e-6;
+constexpr double kOverlapDecodeBytesPerSec = 6.5e12, kOverlapDecodeGain = 2.0;
+
+pkv_status pkv_overlap_prefill_ctas(double prefill_flops, double decode_bytes, int32_t* ctas) {
+  if (!ctas || !std::isfinite(prefill_flops) || !std::isfinite(decode_bytes) ||
+      prefill_flops < 0 || decode_bytes < 0)
+    return PKV_ERR_INVALID;
+  const int all = pkv_host::prefill_ctas(sm_count());
+  const double tp = prefill_flops / kOverlapPrefillFlopsPerSec + kOverlapPrefillFixedSec;
+  const double r = decode_bytes / kOverlapDecodeBytesPerSec / (kOverlapDecodeGain * tp);
+  const int nd = (int)std::lround((double)all * r / (1.0 + r));
+  *ctas = std::max(std::max(1, all / 3), std::min(all, all - nd));
+  return PKV_OK;
+}
+
 pkv_status pkv_paged_attn_prefill(const pkv_pool* pool, const void* q, int32_t total_q,
                                   const int32_t* cu_q,
                                   int32_t batch, int32_t num_q_heads,
                                   const int32_t* block_table, int32_t max_pages,
                                   const int32_t* seq_lens, int32_t max_q_len,
                                   float softmax_scale, void* workspace, size_t workspace_bytes,
-                                  void* out, float* lse, void* stream) {
+                                  int32_t num_ctas, void* out, float* lse, void* stream) {
   pkv_status st = check_pool(pool);
   if (st != PKV_OK) return st;
   if (batch < 0 || total_q < 0 || num_q_heads <= 0 || num_q_heads % pool->num_kv_heads ||
-      max_pages <= 0 || max_q_len < 0 || !std::isfinite(softmax_scale))
+      max_pages <= 0 || max_q_len < 0 || !std::isfinite(softmax_scale) || num_ctas < 0)
     return PKV_ERR_INVALID;
   if (pool->dtype != PKV_BF16) return PKV_ERR_UNSUPPORTED;
   if (batch == 0 || max_q_len == 0 || total_q == 0) return PKV_OK;
   if (!q || !cu_q || !block_table || !seq_lens || !out) return PKV_ERR_INVALID;
   if (!aligned(q, 16) || !aligned(out, 16)) return PKV_ERR_INVALID;
   if (batch > 65535 || num_q_heads > 65535) return PKV_ERR_UNSUPPORTED;
-  const int ctas = pkv_host::prefill_ctas(sm_count());
+  const int all = pkv_host::prefill_ctas(sm_count());
+  const int ctas = num_ctas > 0 && num_ctas < all ? num_ctas : all;
+  // the workspace is laid out for every SM whatever num_ctas is
   if (!workspace || !aligned(workspace, 16) ||
-      workspace_bytes < pkv_host::prefill_workspace_bytes(ctas))
+      workspace_bytes < pkv_host::prefill_workspace_bytes(all))
     return PKV_ERR_INVALID;
   pkv_host::PrefillLaunch a{pool->k, pool->v, pool->num_pages, pool->num_kv_heads, q, total_q,
                             cu_q, batch, num_q_heads, block_table, max_pages, seq_lens, max_q_len,
-                            softmax_scale, out, lse, ctas, workspace};
+                            softmax_scale, out, lse, ctas, workspace, all};
   cudaError_t e = pkv_host::launch_prefill(a, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return PKV_ERR_UNSUPPORTED;
   return cuda_status(e);

@@ -114,8 +114,11 @@ struct PrefillLaunch {
   float softmax_scale;
   void* out;
   float* lse;
-  int ctas;                // persistent CTAs (one per SM)
-  void* workspace;         // prefill_workspace_bytes(ctas) bytes, 16-byte aligned
+  int ctas;                // persistent CTAs (at most one per SM)
+  void* workspace;         // prefill_workspace_bytes(ws_ctas) bytes, 16-byte aligned
+  int ws_ctas;             // the CTA count the workspace is laid out for (>= ctas): the
+                           // same for every call, whatever its ctas, so that one call's
+                           // partial results never sit where another's counters go
 };
 
 constexpr int kMaxPrefillCtas = 1024;

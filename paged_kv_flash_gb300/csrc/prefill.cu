@@ -999,7 +999,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         // The whole S row in one round trip; packed P then overwrites the S
         // registers it came from (c <= 2c) and goes to TMEM columns 64..127
-        // of S_x, which are consumed by then.
+        // of S_x, which are consumed by then: its first half (keys 0..63) as
+        // soon as it is complete, so that the store overlaps the second.
         const int kbase = j * BN;
         uint32_t sr[128];
         tmem_ld64(t_lane + tm_s(x), *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
@@ -1030,8 +1031,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const float2 pp = make_float2(fast_exp2(tv2.x), fast_exp2(tv2.y));
           sum2[cc & 1] = add2(sum2[cc & 1], pp);
           sr[cc] = pack_bf16x2(pp.x, pp.y);
+          if (cc == BN / 4 - 1)
+            tmem_st32(t_lane + tm_p(x), *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
         }
-        tmem_st64(t_lane + tm_p(x), *reinterpret_cast<const uint32_t(*)[64]>(&sr[0]));
+        tmem_st32(t_lane + tm_p(x) + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
         const float2 s2 = add2(sum2[0], sum2[1]);
         l_run = l_run * alpha + (s2.x + s2.y);
         m_run = m_use;
@@ -1337,11 +1340,13 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t s) {
     cudaError_t e = pkv_host::set_max_dynamic_smem(reinterpret_cast<const void*>(fn), SMEM_BYTES);
     if (e != cudaSuccess) return e;
   }
-  if (a.ctas <= 0 || a.ctas > kMaxPrefillCtas || !a.workspace) return cudaErrorInvalidValue;
+  if (a.ctas <= 0 || a.ctas > a.ws_ctas || a.ws_ctas > kMaxPrefillCtas || !a.workspace)
+    return cudaErrorInvalidValue;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const int n = a.ws_ctas;
   PrefillParams prm{a, reinterpret_cast<uint32_t*>(ws),
-                    reinterpret_cast<float*>(ws + ws_counter_bytes(a.ctas)),
-                    reinterpret_cast<float4*>(ws + ws_counter_bytes(a.ctas) + ws_lse_bytes(a.ctas))};
+                    reinterpret_cast<float*>(ws + ws_counter_bytes(n)),
+                    reinterpret_cast<float4*>(ws + ws_counter_bytes(n) + ws_lse_bytes(n))};
   // The head-pair build (units of two heads on one row tile) only where a
   // chunk ends in a single row tile: max_q_len tells it exactly for one
   // sequence and is a proxy for a batch; either build is correct for any

@@ -43,7 +43,7 @@ _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size
 _POOLP = ctypes.POINTER(_Pool)
 SIGNATURES = {
     "pkv_kv_append": (_I, [_POOLP, _P, _P, _I, _P, _I, _P, _I, _P, _P, _P]),
-    "pkv_decode_plan": (_I, [_I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
+    "pkv_decode_plan": (_I, [_I, _I, _I, _I, _I, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
                              ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
     "pkv_paged_attn_decode": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P, _SZ,
                                    _P, _P, _P]),
@@ -52,8 +52,9 @@ SIGNATURES = {
     "pkv_paged_attn_decode_noalloc": (_I, [_POOLP, _P, _I, _I, _P, _I, _P, _I, _F, _P, _I, _P,
                                            _P, _P]),
     "pkv_prefill_plan": (_I, [ctypes.POINTER(_I), ctypes.POINTER(_SZ), ctypes.POINTER(_SZ)]),
-    "pkv_paged_attn_prefill": (_I, [_POOLP, _P, _I, _P, _I, _I, _P, _I, _P, _I, _F, _P, _SZ, _P,
-                                    _P, _P]),
+    "pkv_paged_attn_prefill": (_I, [_POOLP, _P, _I, _P, _I, _I, _P, _I, _P, _I, _F, _P, _SZ, _I,
+                                    _P, _P, _P]),
+    "pkv_overlap_prefill_ctas": (_I, [ctypes.c_double, ctypes.c_double, ctypes.POINTER(_I)]),
     "pkv_decode_multi_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_I),
                                    ctypes.POINTER(_I), ctypes.POINTER(_SZ)]),
     "pkv_paged_attn_decode_multi": (_I, [_POOLP, _P, _I, _P, _I, _I, _P, _I, _P, _I, _I, _F, _I,
@@ -163,11 +164,13 @@ def kv_append(pool: Pool, k_new, v_new, cu_new, block_table, seq_lens, k_smooth=
     _check(st, "pkv_kv_append")
 
 
-def decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits=0):
-    """(splits, pages_per_split, workspace_bytes, zero_bytes) of a decode call."""
+def decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits=0, dtype=BF16):
+    """(splits, pages_per_split, workspace_bytes, zero_bytes) of a decode call
+    on a pool of the given dtype (BF16 or INT8)."""
     s, c, w, z = _I(), _I(), _SZ(), _SZ()
-    st = _lib.pkv_decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, num_splits,
-                              ctypes.byref(s), ctypes.byref(c), ctypes.byref(w), ctypes.byref(z))
+    st = _lib.pkv_decode_plan(batch, num_q_heads, num_kv_heads, max_seq_len, int(dtype),
+                              num_splits, ctypes.byref(s), ctypes.byref(c), ctypes.byref(w),
+                              ctypes.byref(z))
     _check(st, "pkv_decode_plan")
     return s.value, c.value, w.value, z.value
 
@@ -193,7 +196,8 @@ def paged_attn_decode(pool: Pool, q, block_table, seq_lens, max_seq_len, softmax
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
     B, Hq, _ = q.shape
-    _, _, ws_bytes, zero_bytes = decode_plan(B, Hq, pool.num_kv_heads, max_seq_len, num_splits)
+    _, _, ws_bytes, zero_bytes = decode_plan(B, Hq, pool.num_kv_heads, max_seq_len, num_splits,
+                                             pool.dtype)
     if workspace is None and ws_bytes:
         workspace = decode_workspace(ws_bytes, zero_bytes, q.device)
     if out is None:
@@ -254,9 +258,11 @@ def prefill_workspace(device="cuda"):
 
 
 def paged_attn_prefill(pool: Pool, q, cu_q, block_table, seq_lens, max_q_len, softmax_scale,
-                       workspace=None, out=None, lse=None, want_lse=True, stream=None):
+                       workspace=None, out=None, lse=None, want_lse=True, stream=None,
+                       num_ctas=0):
     """Causal chunk attention: q [total_q][Hq][128] bf16 -> (out bf16, lse fp32).
-    `workspace` (from prefill_workspace()) is allocated when not given."""
+    `workspace` (from prefill_workspace()) is allocated when not given.
+    num_ctas: persistent CTAs, 0 = one per SM (see overlap_prefill_ctas)."""
     _need(q, torch.bfloat16, "q")
     for t, n in ((cu_q, "cu_q"), (block_table, "block_table"), (seq_lens, "seq_lens")):
         _need(t, torch.int32, n)
@@ -271,10 +277,19 @@ def paged_attn_prefill(pool: Pool, q, cu_q, block_table, seq_lens, max_q_len, so
     st = _lib.pkv_paged_attn_prefill(
         ctypes.byref(pc), _ptr(q), T, _ptr(cu_q), seq_lens.shape[0], Hq, _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), int(max_q_len), float(softmax_scale),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse),
-        _stream(stream))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), int(num_ctas), _ptr(out),
+        _ptr(lse), _stream(stream))
     _check(st, "pkv_paged_attn_prefill")
     return out, lse
+
+
+def overlap_prefill_ctas(prefill_flops, decode_bytes):
+    """num_ctas for a prefill that runs beside a decode on another stream
+    (see pkv_overlap_prefill_ctas)."""
+    n = _I()
+    _check(_lib.pkv_overlap_prefill_ctas(float(prefill_flops), float(decode_bytes),
+                                         ctypes.byref(n)), "pkv_overlap_prefill_ctas")
+    return n.value
 
 
 def decode_multi_plan(batch, total_q, num_q_heads, num_kv_heads, max_q_len, max_seq_len,

@@ -94,7 +94,7 @@ def test_decode_rejects_short_workspace(lib):
     # four splits of one page each need a workspace; none given
     assert decode(lib, good_pool(), splits=4) == INVALID
     s, c, w, z = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
-    assert lib.pkv_decode_plan(1, 4, 2, 64, 4, ctypes.byref(s), ctypes.byref(c),
+    assert lib.pkv_decode_plan(1, 4, 2, 64, 0, 4, ctypes.byref(s), ctypes.byref(c),
                                ctypes.byref(w), ctypes.byref(z)) == 0
     assert (s.value, c.value) == (4, 1) and w.value > 0
     assert z.value == 65536 * 4                 # fixed counter region
@@ -105,10 +105,10 @@ def test_decode_rejects_short_workspace(lib):
 def test_forced_split_beyond_counter_region_is_rejected(lib):
     s, c, w, z = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
     # 8,193 sequences x 8 KV heads > 65,536 counters
-    assert lib.pkv_decode_plan(8193, 32, 8, 4096, 4, ctypes.byref(s), ctypes.byref(c),
+    assert lib.pkv_decode_plan(8193, 32, 8, 4096, 0, 4, ctypes.byref(s), ctypes.byref(c),
                                ctypes.byref(w), ctypes.byref(z)) == INVALID
     # the heuristic does not split them
-    assert lib.pkv_decode_plan(8193, 32, 8, 4096, 0, ctypes.byref(s), ctypes.byref(c),
+    assert lib.pkv_decode_plan(8193, 32, 8, 4096, 0, 0, ctypes.byref(s), ctypes.byref(c),
                                ctypes.byref(w), ctypes.byref(z)) == 0
     assert s.value == 1 and w.value == 0 and z.value == 0
 
@@ -124,15 +124,27 @@ def test_decode_empty_batch_is_a_no_op(lib):
 def test_plan_heuristic_bounds(lib):
     s, c, w, z = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
     for B, Hkv, L in [(1, 8, 1024), (64, 8, 8192), (1, 8, 32768), (8, 8, 32768), (32, 8, 16398)]:
-        assert lib.pkv_decode_plan(B, 4 * Hkv, Hkv, L, 0, ctypes.byref(s), ctypes.byref(c),
-                                   ctypes.byref(w), ctypes.byref(z)) == 0
-        pages = (L + 15) // 16
-        assert 1 <= c.value <= 128 and s.value == -(-pages // c.value)
-        if s.value > 1:
-            assert z.value == 65536 * 4
-            assert w.value >= z.value + B * 4 * Hkv * s.value * 129 * 4
-        else:
-            assert w.value == 0 and z.value == 0
+        ws_of = {}
+        for dtype, cap in ((0, 96), (1, 128)):
+            assert lib.pkv_decode_plan(B, 4 * Hkv, Hkv, L, dtype, 0, ctypes.byref(s),
+                                       ctypes.byref(c), ctypes.byref(w), ctypes.byref(z)) == 0
+            pages = (L + 15) // 16
+            assert 1 <= c.value <= cap and s.value == -(-pages // c.value)
+            if s.value > 1:
+                assert z.value == 65536 * 4
+                assert w.value >= z.value + B * 4 * Hkv * s.value * 129 * 4
+            else:
+                assert w.value == 0 and z.value == 0
+            ws_of[dtype] = w.value
+        # the bf16 plan's workspace serves an INT8 pool of the same shape
+        assert ws_of[0] >= ws_of[1]
+
+
+def test_plan_rejects_unknown_dtype(lib):
+    s, c, w, z = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
+    for dtype in (-1, 2):
+        assert lib.pkv_decode_plan(1, 4, 2, 64, dtype, 0, ctypes.byref(s), ctypes.byref(c),
+                                   ctypes.byref(w), ctypes.byref(z)) == INVALID
 
 
 def test_append_rejects_bad_arguments(lib):
@@ -165,7 +177,7 @@ def test_prefill_rejects_int8_pool_and_bad_arguments(lib):
     assert zb.value == (8 * ctas.value + 255) // 256 * 256
     assert ws.value == zb.value + ctas.value * 256 * 129 * 4
     args = [V(FAKE), 16, V(FAKE), 1, 4, V(FAKE), 4, V(FAKE), 16, ctypes.c_float(0.1), V(FAKE),
-            ctypes.c_size_t(ws.value), V(FAKE), None, None]
+            ctypes.c_size_t(ws.value), 0, V(FAKE), None, None]
     assert f(ctypes.byref(i8), *args) == UNSUPPORTED
     bf = good_pool()
     bad = list(args)
@@ -186,6 +198,29 @@ def test_prefill_rejects_int8_pool_and_bad_arguments(lib):
     none = list(args)
     none[1] = 0                                                 # no query rows: nothing to do
     assert f(ctypes.byref(bf), *none) == 0
+    negc = list(args)
+    negc[12] = -1                                               # negative CTA count
+    assert f(ctypes.byref(bf), *negc) == INVALID
+
+
+def test_overlap_split_bounds_and_order(lib):
+    f = lib.pkv_overlap_prefill_ctas
+    f.restype = ctypes.c_int32
+    f.argtypes = [ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_int32)]
+    all_ = ctypes.c_int32()
+    assert lib.pkv_prefill_plan(ctypes.byref(all_), None, None) == 0
+    n = ctypes.c_int32()
+    got = []
+    for flops in (0.0, 1e10, 1e11, 1e12, 1e13, 1e15):
+        assert f(flops, 1.26e9, ctypes.byref(n)) == 0
+        assert max(1, all_.value // 3) <= n.value <= all_.value
+        got.append(n.value)
+    assert got == sorted(got)                   # more prefill work: more of the SMs
+    assert got[-1] > got[0]
+    assert f(1e12, 0.0, ctypes.byref(n)) == 0 and n.value == all_.value   # no decode: all SMs
+    for bad in ((-1.0, 1e9), (1e12, -1.0), (float("nan"), 1e9), (1e12, float("inf"))):
+        assert f(*bad, ctypes.byref(n)) == INVALID
+    assert f(1e12, 1e9, None) == INVALID
 
 
 def test_status_strings(lib):

@@ -39,6 +39,32 @@ def test_frac_uses_the_burst_peak_for_a_short_region_and_sustained_for_a_long_on
     assert abs(short["frac_clock_normalized"] - 1000.0 / (1953.3 * 2070.0 / 1477.0)) < 1e-4
 
 
+def test_overlapped_schedule_reports_the_prefill_sm_share():
+    r = _r(10.0)
+    r.update(overlap=True, sm_share=0.75)
+    line = bench.make_line(20, 5, 1, r, (1, 1, 1, 28), PEAKS, {}, {})
+    roof = line["roofline"]
+    assert roof["peak"] == 1953.3                      # the measured peak itself
+    assert abs(roof["frac"] - 1000.0 / 1953.3) < 1e-4
+    assert roof["sm_share"] == 0.75
+    assert abs(roof["frac_of_sm_share"] - 1000.0 / 1953.3 / 0.75) < 1e-4
+    assert line["schedule"].startswith("overlapped")
+    seq = bench.make_line(20, 5, 1, _r(10.0), (1, 1, 1, 28), PEAKS, {}, {})
+    assert "sm_share" not in seq["roofline"] and seq["schedule"].startswith("sequential")
+    assert "sequential" not in seq
+    # with the same steps timed one after the other as well
+    alone = _r(10.0, K=280)
+    alone.update(steps=280, pre_ms=0.28 * 280, flops=4.0e11 * 280, dec_ms=0.2 * 280,
+                 dbytes=1.3e9 * 280)
+    r.update(alone=alone)
+    line = bench.make_line(20, 5, 1, r, (1, 1, 1, 28), PEAKS, {}, {})
+    a_tf = 4.0e11 / 0.28e-3 / 1e12
+    assert abs(line["roofline"]["achieved_alone"] - round(a_tf, 1)) < 1e-6
+    assert abs(line["sequential"]["prefill"]["frac_of_measured_burst"] - a_tf / 1953.3) < 1e-4
+    assert abs(line["sequential"]["decode"]["GBps"] - 1.3e9 / 0.2e-3 / 1e9) < 1e-6
+    assert line["sequential"]["steps"] == 280
+
+
 def test_traffic_only_from_a_capture_of_the_current_sources(tmp_path, monkeypatch):
     cur = bench.sources_sha256(bench.PREFILL_SOURCES)
     f = tmp_path / "prof.md"

@@ -2,11 +2,13 @@
 oracle: the bench's own step sequence (one 26,926-token prompt prefilled in
 2,048-row chunks against its cached prefix, plus 32 decode rows with contexts
 ~ U[128, 16384] that gain one token per step, in one shared pool of 16-token
-pages), all 14 steps on one stream: append (chunk rows and one row per
-decode sequence, one call), prefill of the chunk, decode of the 32 rows
-(TileInfer.jl "Performance" page, "Fused kernels, FlashAttention and
-PagedAttention": split-KV decode over the pages in place; "What is left to
-gain": chunked prefill).
+pages), all 14 steps: append (chunk rows and one row per decode sequence,
+one call), then prefill of the chunk and decode of the 32 rows -- one after
+the other on one stream, and overlapped (the prefill on part of the SMs, the
+decode beside it on a second stream, as the bench times it) (TileInfer.jl
+"Performance" page, "Fused kernels, FlashAttention and PagedAttention":
+split-KV decode over the pages in place; "What is left to gain": chunked
+prefill).
 
 At the first, a middle and the last step every decode row (contexts past
 8,192 positions, the split heuristic's plan for 32 rows) and a seeded sample
@@ -23,12 +25,17 @@ from tests.helpers import check_lse, check_out
 pytestmark = pytest.mark.gpu
 
 
-def test_mixed_step_all_fourteen_steps_against_the_oracle():
+@pytest.mark.parametrize("overlap", [True, False], ids=["overlapped", "sequential"])
+def test_mixed_step_all_fourteen_steps_against_the_oracle(overlap):
     import bench
     from paged_kv_flash_gb300 import pagedkv as pk
     from paged_kv_flash_gb300 import workloads as W
 
-    mixed = bench.Mixed(torch, pk)
+    mixed = bench.Mixed(torch, pk, overlap=overlap)
+    if overlap:
+        all_ctas = pk.prefill_plan()[0]
+        ctas = [st["ctas"] for st in mixed.steps]
+        assert all(1 <= n <= all_ctas for n in ctas) and min(ctas) < all_ctas
     wl = mixed.wl
     assert len(wl.steps) == 14 and len(wl.decode_lens0) == 32
     assert int(wl.steps[0].decode_lens.max()) > 8192
@@ -39,7 +46,7 @@ def test_mixed_step_all_fourteen_steps_against_the_oracle():
     checked = {0, 7, 13}
     R = len(wl.decode_lens0)
     for c, s in enumerate(wl.steps):
-        mixed.step(c)                              # append -> prefill -> decode, one stream
+        mixed.step(c)                              # append, then prefill and decode
         cu_app, lens_app = wl.step_append(s)
         kp, vp = oracle.kv_append_bf16(kp, vp, s.k_new, s.v_new, cu_app, bt, lens_app)
         if c not in checked:

@@ -225,3 +225,28 @@ def test_workspace_reuse_is_exact(pk):
             assert torch.equal(o, o0) and torch.equal(l, l0)
     assert pk.poll_device_error() == pk.OK
     assert int(ws[:zero_bytes].count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("num_ctas", [1, 7, 61])
+def test_fewer_persistent_ctas(pk, num_ctas):
+    """num_ctas below the SM count (the prefill beside a decode on another
+    stream): the same work in fewer persistent CTAs -- whole units, cut
+    units and a head-pair chunk tail -- matches the oracle and leaves the
+    workspace's part counters at zero; a call on every SM with units cut
+    over many CTAs then shares that workspace and still matches (the
+    partial results of the first call never sit where its counters go)."""
+    rng = np.random.default_rng(68 + num_ctas)
+    ws = pk.prefill_workspace()
+    zero_bytes = pk.prefill_plan()[2]
+    for shapes, n in (([(1000, 3000), (130, 4100), (33, 90), (1, 700)], num_ctas),
+                      ([(256, 8192), (700, 2000)], 0)):
+        case, q, cu, mq = chunk_case(rng, shapes, Hq=8, Hkv=2)
+        pool = pk.Pool(dev_bf16(case.k_pool), dev_bf16(case.v_pool))
+        out, lse = pk.paged_attn_prefill(pool, dev_bf16(q), dev(cu),
+                                         dev(case.layout.block_table), dev(case.seq_lens), mq,
+                                         case.scale, workspace=ws, num_ctas=n)
+        assert pk.poll_device_error() == pk.OK
+        ro, rl = ref(case, q, cu)
+        check_out(out, ro, f"{n} CTAs")
+        check_lse(lse, rl, f"{n} CTAs")
+        assert int(ws[:zero_bytes].count_nonzero()) == 0
