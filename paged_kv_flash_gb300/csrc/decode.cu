@@ -192,13 +192,33 @@ __global__ void __launch_bounds__(bfmma::W * 32, 2)
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int Hq = a.num_q_heads;
 
+  // Every load that needs nothing else goes out first, so that their
+  // latencies overlap: the length, this warp's first 32 page ids (any entry
+  // of the table row is in bounds; those past the sequence are not used)
+  // and the query rows as B fragments (column r = head r of the group, zero
+  // for r >= G; rows = channels 16 ks + 2qd, + 1 (qb[ks][0]) and + 8, + 9).
+  const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
+  const int p_begin = split * a.pages_per_split;
   int L = a.seq_lens[b];
+  const int lp0 = p_begin + warp + lane * W;
+  const int bt_first = lp0 < a.max_pages ? __ldg(bt_row + lp0) : 0;
+  uint32_t qb[8][2];
+  {
+    const bool valid = r < G;
+    const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
+                                ((size_t)b * Hq + h * G + (valid ? r : 0)) * kHeadDim;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      qb[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * qd)) : 0u;
+      qb[ks][1] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * qd))
+                        : 0u;
+    }
+  }
   if (L < 0 || L > a.max_pages * kPageSize) {
     if (threadIdx.x == 0) atomicOr(&g_err_decode, kErrBadIndex);
     L = 0;
   }
   const int npages = (L + kPageSize - 1) / kPageSize;
-  const int p_begin = split * a.pages_per_split;
   if (split > 0 && p_begin >= npages) return;   // empty split: the merge skips it
   // splits holding keys (split 0 always runs); with one, it writes the output
   const int nv = max(1, (npages + a.pages_per_split - 1) / a.pages_per_split);
@@ -216,14 +236,14 @@ __global__ void __launch_bounds__(bfmma::W * 32, 2)
   }
   __syncwarp();
 
-  // Page ids of this warp's pages, 32 at a time, one per lane.
-  const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
+  // Page ids of this warp's pages, 32 at a time, one per lane (the first 32
+  // loaded above).
   const uint64_t policy = l2_policy_evict_first();
   int bt_cache = 0;
   auto page_id = [&](int i) -> int {
     if ((i & 31) == 0) {
       const int lp = p_begin + warp + (i + lane) * W;
-      bt_cache = (i + lane < n_w) ? __ldg(bt_row + lp) : 0;
+      bt_cache = (i + lane < n_w) ? (i == 0 ? bt_first : __ldg(bt_row + lp)) : 0;
     }
     int pg = __shfl_sync(FULL, bt_cache, i & 31);
     if (pg < 0 || pg >= a.num_pages) {
@@ -247,25 +267,9 @@ __global__ void __launch_bounds__(bfmma::W * 32, 2)
       tma_box(dst + SLAB + HALF, &tv, 64, row, bar, policy);
     }
   };
-  // the first page copies go out before the query rows are loaded
   const int pro = min(NB, n_w);
   for (int i = 0; i < pro; ++i) issue(i, page_id(i));
   int issued = pro;
-
-  // The query rows as B fragments: column r = head r of the group (zero for
-  // r >= G), rows = channels 16 ks + 2qd, + 1 (qb[ks][0]) and + 8, + 9.
-  uint32_t qb[8][2];
-  {
-    const bool valid = r < G;
-    const __nv_bfloat16* qrow = static_cast<const __nv_bfloat16*>(a.q) +
-                                ((size_t)b * Hq + h * G + (valid ? r : 0)) * kHeadDim;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      qb[ks][0] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * qd)) : 0u;
-      qb[ks][1] = valid ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * qd))
-                        : 0u;
-    }
-  }
   const float sl2 = a.softmax_scale * kLog2e;
   // O^T: channels 16 mt + r (o[mt][0..1]) and + 8 (o[mt][2..3]) of heads 2qd
   // (o[mt][0], o[mt][2]) and 2qd + 1 (o[mt][1], o[mt][3])
@@ -516,13 +520,55 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int Hq = a.num_q_heads;
 
+  // Every load that needs nothing else goes out first, so that their
+  // latencies overlap: the length, this warp's first 32 page ids (any entry
+  // of the table row is in bounds; those past the sequence are not used),
+  // and the query channels and smoothing weights of this lane's A fragments
+  // (row rr < G is head rr's high part, G <= rr < 2G head rr - G's low part;
+  // per k-step kb, channels 32 qd + 4 kb + {0..3} of rows r and r + 8).
+  const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
+  const int p_begin = split * a.pages_per_split;
   int L = a.seq_lens[b];
+  const int lp0 = p_begin + warp + lane * W;
+  const int bt_first = lp0 < a.max_pages ? __ldg(bt_row + lp0) : 0;
+  int qg[2];
+  bool qlow[2];
+  uint2 qraw[2][8];
+  float4 qw[8];
+  {
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int rr = r + 8 * half;
+      int g = -1;
+      bool low = false;
+      if (half == 0 || G == 8) {
+        if (rr < G) {
+          g = rr;
+        } else if (rr < 2 * G) {
+          g = rr - G;
+          low = true;
+        }
+      }
+      qg[half] = g;
+      qlow[half] = low;
+#pragma unroll
+      for (int kb = 0; kb < 8; ++kb)
+        qraw[half][kb] = g >= 0 ? __ldg(reinterpret_cast<const uint2*>(
+                                      qb + ((size_t)b * Hq + h * G + g) * kHeadDim +
+                                      32 * qd + 4 * kb))
+                                : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb)
+      qw[kb] = a.k_smooth ? __ldg(reinterpret_cast<const float4*>(a.k_smooth + 32 * qd + 4 * kb))
+                          : make_float4(1.f, 1.f, 1.f, 1.f);
+  }
   if (L < 0 || L > a.max_pages * kPageSize) {
     if (threadIdx.x == 0) atomicOr(&g_err_decode, kErrBadIndex);
     L = 0;
   }
   const int npages = (L + kPageSize - 1) / kPageSize;
-  const int p_begin = split * a.pages_per_split;
   if (split > 0 && p_begin >= npages) return;   // empty split: the merge skips it
   const int nv = max(1, (npages + a.pages_per_split - 1) / a.pages_per_split);
   const bool direct = a.splits == 1 || nv == 1;
@@ -541,13 +587,12 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
   }
   __syncwarp();
 
-  const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages;
   const uint64_t policy = l2_policy_evict_first();
   int bt_cache = 0;
   auto page_id = [&](int i) -> int {
     if ((i & 31) == 0) {
       const int lp = p_begin + warp + (i + lane) * W;
-      bt_cache = (i + lane < n_w) ? __ldg(bt_row + lp) : 0;
+      bt_cache = (i + lane < n_w) ? (i == 0 ? bt_first : __ldg(bt_row + lp)) : 0;
     }
     int pg = __shfl_sync(FULL, bt_cache, i & 31);
     if (pg < 0 || pg >= a.num_pages) {
@@ -575,49 +620,32 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
   for (int i = 0; i < pro; ++i) issue(i, page_id(i));
   int issued = pro;
 
-  // A fragments of the query: row rr < G is head rr's high part, G <= rr <
-  // 2G head rr - G's low part; per k-step kb, lane (r, qd) holds channels
+  // A fragments of the query (the loads above): lane (r, qd) holds channels
   // 32 qd + 4 kb + {0, 1} (a0a1 / a2a3) and + {2, 3} (a4a5 / a6a7) of rows
-  // r and r + 8.  Pre-scaled by softmax_scale * log2(e) and the key
-  // smoothing weight.
+  // r and r + 8, pre-scaled by softmax_scale * log2(e) and the key smoothing
+  // weight.
   uint32_t qa[8][4];
   {
     const float qs = a.softmax_scale * kLog2e;
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      const int rr = r + 8 * half;
-      int g = -1;
-      bool low = false;
-      if (half == 0 || G == 8) {
-        if (rr < G) {
-          g = rr;
-        } else if (rr < 2 * G) {
-          g = rr - G;
-          low = true;
-        }
-      }
 #pragma unroll
       for (int kb = 0; kb < 8; ++kb) {
         uint32_t v01 = 0, v23 = 0;
-        if (g >= 0) {
-          const int c0 = 32 * qd + 4 * kb;
-          const uint2 raw = __ldg(reinterpret_cast<const uint2*>(
-              qb + ((size_t)b * Hq + h * G + g) * kHeadDim + c0));
+        if (qg[half] >= 0) {
+          const uint2 raw = qraw[half][kb];
           float x[4] = {bf16lo(raw.x) * qs, bf16hi(raw.x) * qs, bf16lo(raw.y) * qs,
                         bf16hi(raw.y) * qs};
           if (a.k_smooth) {
-            const float2 w01 = __ldg(reinterpret_cast<const float2*>(a.k_smooth + c0));
-            const float2 w23 = __ldg(reinterpret_cast<const float2*>(a.k_smooth + c0 + 2));
-            x[0] *= w01.x;
-            x[1] *= w01.y;
-            x[2] *= w23.x;
-            x[3] *= w23.y;
+            x[0] *= qw[kb].x;
+            x[1] *= qw[kb].y;
+            x[2] *= qw[kb].z;
+            x[3] *= qw[kb].w;
           }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float hi = __half2float(__float2half_rn(x[e]));
-            x[e] = low ? x[e] - hi : hi;
+            x[e] = qlow[half] ? x[e] - hi : hi;
           }
           v01 = pack_f16x2(x[0], x[1]);
           v23 = pack_f16x2(x[2], x[3]);

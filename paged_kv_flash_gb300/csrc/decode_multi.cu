@@ -102,6 +102,12 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int h = blockIdx.y / a.row_groups, rg = blockIdx.y % a.row_groups;
   const int b = blockIdx.z;
 
+  // The producer's first 32 page ids go out with the lengths (any entry of
+  // the table row is in bounds; those past the sequence are not used).
+  const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages + split * a.pages_per_split;
+  int bt_first = 0;
+  if (warp == kConsumers && split * a.pages_per_split + lane < a.max_pages)
+    bt_first = __ldg(bt_row + lane);
   const int q0 = a.cu_q[b], qn = a.cu_q[b + 1] - q0;
   const int L = a.seq_lens[b];
   if (qn < 0 || qn > a.max_q || L < qn || L > a.max_pages * kPageSize) {
@@ -147,11 +153,11 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   if (warp == kConsumers) {
     // ---------------------------------------------------------- producer
-    const int32_t* bt_row = a.block_table + (size_t)b * a.max_pages + p_begin;
     const uint64_t policy = l2_policy_evict_first();
     int bt_cache = 0, issued = 0;
     for (int i = 0; i < n_pages; ++i) {
-      if ((i & 31) == 0) bt_cache = (i + lane < n_pages) ? __ldg(bt_row + i + lane) : 0;
+      if ((i & 31) == 0)
+        bt_cache = (i + lane < n_pages) ? (i == 0 ? bt_first : __ldg(bt_row + i + lane)) : 0;
       int pg = __shfl_sync(FULL, bt_cache, i & 31);
       if (pg < 0 || pg >= a.num_pages) {
         if (lane == 0) atomicOr(&g_err_multi, kErrBadIndex);
