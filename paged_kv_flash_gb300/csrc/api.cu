@@ -77,8 +77,9 @@ pkv_status check_pool(const pkv_pool* pool) {
 
 // Split plan: pages per split C and split count S for a decode call.
 //
-// The split kernel runs one CTA per (split, KV head, sequence) with 4 warps,
-// two CTAs resident per SM.  A CTA pays a few microseconds of start-up
+// The split kernel runs one CTA per (split, KV head, sequence) with 4 warps
+// (bf16, three CTAs resident per SM) or 8 (INT8, two); the plan counts two
+// resident CTAs per SM for both.  A CTA pays a few microseconds of start-up
 // (query and block-table loads, the first page copies), so splits are made
 // as long as the machine allows: about 0.8 CTAs per resident slot, estimated
 // from the longest sequence, with 8 to 96 bf16 pages or 8 to 128 INT8 pages

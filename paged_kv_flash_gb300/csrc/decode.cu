@@ -52,14 +52,22 @@ __device__ uint32_t g_err_decode;
 // the MMA (0 x NaN would reach O).
 namespace bfmma {
 
+// Three CTAs of 4 warps per SM, 2 page buffers per warp: as many bytes in
+// flight per SM as two CTAs with 3 buffers per warp, and half again as many
+// warps to work on the pages that have landed.  On the whole GPU the kernel
+// is HBM-bound either way; on a few SMs beside a prefill (a continuous-
+// batching step) the work per page sets its pace, and there the extra warps
+// took the mixed step from 424 to 402 us (the decode alone: unchanged).
 constexpr int W = pkv_host::kDecodeWarps;               // warps per CTA, pages round-robin
-constexpr int NB = 3;                                   // page buffers per warp
+constexpr int NB = 2;                                   // page buffers per warp
+constexpr int CTAS_PER_SM = 3;                          // resident CTAs (shared memory)
 constexpr int HALF = kPageSize * 128;                   // one box: 16 keys x 64 bf16
 constexpr int SLAB = 2 * HALF;                          // K or V of one (page, head)
 constexpr int PAGE = 2 * SLAB;                          // K, then V
 constexpr int WARP_BYTES = NB * PAGE;
 constexpr int SMEM = 1024 + W * WARP_BYTES;
 static_assert(W * NB * 8 <= 1016, "barriers fit the header");
+static_assert(CTAS_PER_SM * (SMEM + 1024) <= 228 * 1024, "resident CTAs fit shared memory");
 
 // The 16-byte chunk holding channels ch .. ch + 7 of key row `key` of a slab:
 // two 64-channel halves, chunk c of row k at c ^ (k & 7).
@@ -177,7 +185,7 @@ __device__ __forceinline__ void merge_warps(const pkv_host::DecodeLaunch& a, uin
 // (a.ws_ctr counts them); otherwise a separate combine kernel does.  A
 // template parameter, so that the default kernel carries none of that code.
 template <int G, bool FUSED>
-__global__ void __launch_bounds__(bfmma::W * 32, 2)
+__global__ void __launch_bounds__(bfmma::W * 32, bfmma::CTAS_PER_SM)
     decode_split_kernel(const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv,
                         const __grid_constant__ pkv_host::DecodeLaunch a) {

@@ -52,7 +52,7 @@ struct DecodeLaunch {
 
 // Kernel geometry the split heuristic needs.
 constexpr int kDecodeWarps = 4;          // warps per split CTA
-constexpr int kDecodeCtasPerSm = 2;      // resident split CTAs per SM (by smem)
+constexpr int kDecodeCtasPerSm = 2;      // split CTAs per SM the plan counts on
 
 // cuTensorMapEncodeTiled of an INT8 pool (K or V) as 2-D uint8 rows of 128
 // bytes, one box per (page, head) slab of 16 rows, 128B-swizzled; `map`
