@@ -102,9 +102,10 @@ pkv_status pkv_kv_append(const pkv_pool* pool, const void* k_new, const void* v_
 /*
  * Split plan of a decode call ("Fused kernels ...": split-KV for decode).
  * Host-only; launches nothing.  max_seq_len (host) bounds every seq_lens[b];
- * dtype is the pool's pkv_kv_dtype (the heuristic gives INT8 pages, half the
- * bytes, longer splits; a bf16 plan's workspace is never smaller than the
- * INT8 plan's of the same shape); num_splits 0 asks for the built-in
+ * dtype is the pool's pkv_kv_dtype (the heuristic plans the two kernels
+ * differently: INT8 pages, half the bytes, get longer splits, and the INT8
+ * kernel, bound by its work per page, gets a full wave of CTAs); a plan is
+ * for its dtype only; num_splits 0 asks for the built-in
  * heuristic (split count chosen from the batch, the heads, the dtype and the
  * device's SM count), > 0 forces that many splits.
  * Outputs (host pointers, each may be NULL): the split count S, the pages per

@@ -81,7 +81,9 @@ pkv_status check_pool(const pkv_pool* pool) {
 // (bf16, three CTAs resident per SM) or 8 (INT8, two); the plan counts two
 // resident CTAs per SM for both.  A CTA pays a few microseconds of start-up
 // (query and block-table loads, the first page copies), so splits are made
-// as long as the machine allows: about 0.8 CTAs per resident slot, estimated
+// as long as the machine allows: about 0.8 CTAs per resident slot for bf16
+// (bound by HBM) and one for INT8 (bound by the work per page, which an SM
+// with one CTA does not share: one 32k sequence, 248 CTAs -> 296), estimated
 // from the longest sequence, with 8 to 96 bf16 pages or 8 to 128 INT8 pages
 // (half the bytes) per split, a multiple of the 4 warps so that they get
 // equal work.  Measured on GB300: 64 sequences of 512..8,192 positions and
@@ -89,7 +91,7 @@ pkv_status check_pool(const pkv_pool* pool) {
 // 64..96 bf16 pages per split, 8 bf16 sequences of 32,768 positions at 64..96;
 // one 32k-position INT8 sequence at 64 INT8 pages, eight of them at 128.  A
 // forced split count S gives C = ceil(pages / S).
-constexpr long long kPlanSlotsNum = 4, kPlanSlotsDen = 5;   // 0.8 CTAs per slot
+constexpr long long kPlanSlotsNum = 4, kPlanSlotsDen = 5;   // 0.8 CTAs per slot (bf16)
 constexpr long long kPlanMinPages = 8, kPlanMaxPages = 128, kPlanMaxPagesBf16 = 96;
 
 // Workspace (splits > 1): part counters u32 [kDecodeCounters] indexed by
@@ -104,8 +106,7 @@ struct Plan {
   size_t ws_bytes, ws_zero_bytes, ws_o_offset, ws_lse_offset;
 };
 
-// int8: the pool's dtype (longer splits).  The bf16 plan never has fewer
-// splits than the INT8 one, so its workspace covers both.
+// int8: the pool's dtype (longer splits, a full wave of CTAs).
 Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, int num_splits,
                bool int8) {
   const int mp = std::max(1, (max_seq_len + pkv::kPageSize - 1) / pkv::kPageSize);
@@ -115,7 +116,8 @@ Plan make_plan(int batch, int num_q_heads, int num_kv_heads, int max_seq_len, in
   } else {
     const long long slots = (long long)sm_count() * pkv_host::kDecodeCtasPerSm;
     const long long page_heads = (long long)batch * num_kv_heads * mp;
-    const long long target = std::max<long long>(1, slots * kPlanSlotsNum / kPlanSlotsDen);
+    const long long target =
+        std::max<long long>(1, int8 ? slots : slots * kPlanSlotsNum / kPlanSlotsDen);
     long long c = (page_heads + target - 1) / target;
     c = std::max<long long>(kPlanMinPages,
                             std::min<long long>(int8 ? kPlanMaxPages : kPlanMaxPagesBf16, c));

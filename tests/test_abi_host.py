@@ -124,7 +124,6 @@ def test_decode_empty_batch_is_a_no_op(lib):
 def test_plan_heuristic_bounds(lib):
     s, c, w, z = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t(), ctypes.c_size_t()
     for B, Hkv, L in [(1, 8, 1024), (64, 8, 8192), (1, 8, 32768), (8, 8, 32768), (32, 8, 16398)]:
-        ws_of = {}
         for dtype, cap in ((0, 96), (1, 128)):
             assert lib.pkv_decode_plan(B, 4 * Hkv, Hkv, L, dtype, 0, ctypes.byref(s),
                                        ctypes.byref(c), ctypes.byref(w), ctypes.byref(z)) == 0
@@ -135,9 +134,6 @@ def test_plan_heuristic_bounds(lib):
                 assert w.value >= z.value + B * 4 * Hkv * s.value * 129 * 4
             else:
                 assert w.value == 0 and z.value == 0
-            ws_of[dtype] = w.value
-        # the bf16 plan's workspace serves an INT8 pool of the same shape
-        assert ws_of[0] >= ws_of[1]
 
 
 def test_plan_rejects_unknown_dtype(lib):
