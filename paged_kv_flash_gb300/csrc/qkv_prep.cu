@@ -69,12 +69,15 @@ __device__ __forceinline__ float mean_square_rn(const uint32_t (&wa)[4],
   for (int o = 4; o >= 1; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   const int emax = max(1, (int)(mx >> 7));
   unsigned long long acc = 0;
+  // m^2 << (2 (E - Emax) + 40) = (m << (E - Emax + 20))^2: a 32-bit shift
+  // (below 2^28) and one widening multiply-add instead of 64-bit shifts
   const auto add = [&](uint32_t h) {
     h &= 0x7fffu;
     const int E = (int)(h >> 7);
     const uint32_t m = (h & 0x7fu) | (E ? 0x80u : 0u);
-    const int sh = 2 * (max(E, 1) - emax) + 40;
-    if (sh >= 0) acc += (unsigned long long)(m * m) << sh;
+    const int s = max(E, 1) - emax + 20;
+    const uint32_t v = s >= 0 ? m << s : 0u;
+    acc += (unsigned long long)v * v;
   };
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
