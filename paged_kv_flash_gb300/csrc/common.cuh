@@ -52,6 +52,18 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel calls pdl_trigger() to let the
+// next kernel of its stream, when that one is launched with
+// launch_dependent(), be scheduled before it has finished (the trigger takes
+// effect once every CTA has issued it or exited); that kernel calls
+// pdl_wait() before it touches memory: it returns once the previous kernel
+// has completed and its writes are visible.  Both are no-ops without such a
+// launch.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -272,4 +284,24 @@ int sm_count();                 // cached SM count of the current device
 // current device): the attribute belongs to the device's context, so a
 // process flag would skip a second device.  Thread-safe.
 cudaError_t set_max_dynamic_smem(const void* kernel, int bytes);
+
+// Launches kernel k (no dynamic shared memory) after the work queued on s,
+// allowed to start before the previous kernel has finished (programmatic
+// stream serialization): k must call pdl_wait() before it reads what that
+// kernel wrote.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*k)(Params...), dim3 grid, dim3 block, cudaStream_t s,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
 }

@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(bfmma::W * 32, bfmma::CTAS_PER_SM)
                         const __grid_constant__ pkv_host::DecodeLaunch a) {
   using namespace bfmma;
   constexpr uint32_t FULL = 0xffffffffu;
+  pdl_trigger();                                // the combine may be placed now
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* bufs = smem + 1024;
@@ -518,6 +519,7 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
                               const __grid_constant__ pkv_host::DecodeLaunch a) {
   using namespace i8mma;
   constexpr uint32_t FULL = 0xffffffffu;
+  pdl_trigger();                                // the combine may be placed now
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   uint8_t* bufs = smem + 1024;
@@ -853,6 +855,7 @@ __global__ void __launch_bounds__(i8mma::W * 32, 2)
 __global__ void __launch_bounds__(128) decode_combine_kernel(const __grid_constant__
                                                              pkv_host::DecodeLaunch a) {
   __shared__ float wsm[128], red[4];
+  pdl_wait();                                   // the split kernel's partials
   const int bh = blockIdx.x;
   const int b = bh / a.num_q_heads;
   const int d = threadIdx.x;
@@ -940,8 +943,9 @@ cudaError_t launch_decode(const DecodeLaunch& a, bool int8, cudaStream_t s) {
   if (a.batch == 0) return cudaSuccess;
   cudaError_t e = int8 ? dispatch_i8mma(a, s) : dispatch_group(a, s);
   if (e != cudaSuccess || a.splits == 1 || a.ws_ctr) return e;
-  decode_combine_kernel<<<a.batch * a.num_q_heads, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  // the combine's CTAs are placed while the split kernel's last ones run and
+  // wait on the device for its partials, instead of a launch after it
+  return launch_dependent(decode_combine_kernel, dim3(a.batch * a.num_q_heads), dim3(128), s, a);
 }
 
 uint32_t take_decode_error(cudaStream_t s) { return take_error_word(&g_err_decode, s); }

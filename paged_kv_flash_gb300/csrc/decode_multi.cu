@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(kThreads, 3)
                         const __grid_constant__ CUtensorMap tv,
                         const __grid_constant__ pkv_host::MultiLaunch a) {
   constexpr uint32_t FULL = 0xffffffffu;
+  pdl_trigger();                                // the combine may be placed now
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);          // full [NS], empty [NS]
   volatile uint32_t* abort = reinterpret_cast<volatile uint32_t*>(smem + 1016);
@@ -431,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 3)
 __global__ void __launch_bounds__(128)
     decode_multi_combine_kernel(const __grid_constant__ pkv_host::MultiLaunch a) {
   __shared__ float wsm[128], red[4];
+  pdl_wait();                                   // the split kernel's partials
   const int bh = blockIdx.x;
   const int t = bh / a.num_q_heads;
   const int b = owner_seq(a.cu_q, a.batch, t);
@@ -465,8 +467,9 @@ cudaError_t launch_decode_multi(const MultiLaunch& a, cudaStream_t s) {
   decode_multi_kernel<<<grid, kThreads, SMEM, s>>>(tk, tv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
-  decode_multi_combine_kernel<<<a.total_q * a.num_q_heads, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  // placed while the split kernel's last CTAs run; waits for its partials
+  return pkv_host::launch_dependent(decode_multi_combine_kernel, dim3(a.total_q * a.num_q_heads),
+                                    dim3(128), s, a);
 }
 
 uint32_t take_multi_error(cudaStream_t s) { return take_error_word(&g_err_multi, s); }
