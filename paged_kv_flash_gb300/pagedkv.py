@@ -129,11 +129,17 @@ class Pool:
         return self.k.shape[1]
 
     def c(self) -> _Pool:
-        return _Pool(self.k.data_ptr(), self.v.data_ptr(),
-                     self.k_scale.data_ptr() if self.k_scale is not None else None,
-                     self.v_scale.data_ptr() if self.v_scale is not None else None,
-                     self.k.shape[0], self.k.shape[1], self.k.shape[2], self.k.shape[3],
-                     self.dtype)
+        """The C struct of the pool, rebuilt only when a tensor has changed
+        (it is passed on every call, and a serving loop makes many)."""
+        key = (self.k.data_ptr(), self.v.data_ptr(),
+               self.k_scale.data_ptr() if self.k_scale is not None else None,
+               self.v_scale.data_ptr() if self.v_scale is not None else None,
+               tuple(self.k.shape), self.dtype)
+        cached = self.__dict__.get("_c")
+        if cached is None or cached[0] != key:
+            cached = (key, _Pool(key[0], key[1], key[2], key[3], *key[4], key[5]))
+            self.__dict__["_c"] = cached
+        return cached[1]
 
     @staticmethod
     def empty(num_pages: int, num_kv_heads: int, dtype=torch.bfloat16, device="cuda"):
@@ -196,10 +202,11 @@ def paged_attn_decode(pool: Pool, q, block_table, seq_lens, max_seq_len, softmax
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
     B, Hq, _ = q.shape
-    _, _, ws_bytes, zero_bytes = decode_plan(B, Hq, pool.num_kv_heads, max_seq_len, num_splits,
-                                             pool.dtype)
-    if workspace is None and ws_bytes:
-        workspace = decode_workspace(ws_bytes, zero_bytes, q.device)
+    if workspace is None:                   # (a given workspace's size is checked by the call)
+        _, _, ws_bytes, zero_bytes = decode_plan(B, Hq, pool.num_kv_heads, max_seq_len,
+                                                 num_splits, pool.dtype)
+        if ws_bytes:
+            workspace = decode_workspace(ws_bytes, zero_bytes, q.device)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
