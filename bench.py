@@ -432,14 +432,16 @@ def time_e2e(torch, pk, mixed, K, first):
             if i + 1 < start + n_iter:
                 upload(i + 1)
             run(i)
+        t_enq = time.perf_counter()                # everything queued; the GPU still runs
         torch.cuda.synchronize()
+        return t_enq
 
     loop(first, nsteps)                            # warm-up pass over every chunk
     counts["h2d"] = counts["d2h"] = 0
     t0 = time.perf_counter()
-    loop(first, K)
+    t_enq = loop(first, K)
     dt = time.perf_counter() - t0
-    return dt * 1e6 / K, counts["h2d"] // K, counts["d2h"] // K
+    return dt * 1e6 / K, counts["h2d"] // K, counts["d2h"] // K, (t_enq - t0) * 1e6 / K
 
 
 # ------------------------------------------------------ other workloads
@@ -890,7 +892,8 @@ def make_line(K, Wu, world, r, e2e, peaks_, prof, config, nsteps=14):
     the end-to-end result e2e = (us, h2d bytes, d2h bytes, steps), the peaks
     (peaks()) and the prefill profile figures (prefill_profile())."""
     hbm, bf16, bf16_sus, peak_src, peak_mhz = peaks_
-    e2e_us, h2d, d2h, K_e2e = e2e
+    e2e_us, h2d, d2h, K_e2e = e2e[:4]
+    host_us = e2e[4] if len(e2e) > 4 else None
     us_per_step = r["step_ms"] * 1e3
     pre_tflops = r["flops"] / (r["pre_ms"] * 1e-3) / 1e12
     dec_gbs = r["dbytes"] / (r["dec_ms"] * 1e-3) / 1e9
@@ -980,7 +983,8 @@ def make_line(K, Wu, world, r, e2e, peaks_, prof, config, nsteps=14):
                 "d2h_bytes_per_step": int(d2h), "steps": K_e2e,
                 "note": (f"steps {Wu}..{Wu + K_e2e - 1} (whole passes over the 14 chunks) through "
                          "the public API, inputs from pinned host memory each step, outputs read "
-                         "back each step; wall clock")},
+                         "back each step; wall clock"),
+                "host_enqueue_us_per_step": round(host_us, 2) if host_us is not None else None},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
@@ -1107,9 +1111,9 @@ def main(argv=None):
         r["alone"] = time_mixed(torch, pk, mixed, 20 * nsteps, nsteps, world, rank)
         mixed.overlap = True
     K_e2e = -(-K // nsteps) * nsteps               # whole passes over the 14 chunks
-    e2e_us, h2d, d2h = time_e2e(torch, pk, mixed, K_e2e, Wu)
+    e2e_us, h2d, d2h, host_us = time_e2e(torch, pk, mixed, K_e2e, Wu)
 
-    e2e = (e2e_us, h2d, d2h, K_e2e)
+    e2e = (e2e_us, h2d, d2h, K_e2e, host_us)
     line = make_line(K, Wu, world, r, e2e, (hbm, bf16, bf16_sus, peak_src, peak_mhz),
                      prefill_profile(), config, nsteps)
     if rank == 0 and world == 1 and not args.no_configs:
