@@ -24,8 +24,10 @@ prefill TFLOP/s; the roofline object is for the prefill kernel, which
 dominates the step, with the share of the SMs it held.  "configs" holds
 the other workloads (single-sequence decode, 1,024-token prefill, batched
 decode, INT8 32k decode, 16-token verify steps through the multi-token
-decode, the fused attention-input step on a 2,048-token chunk) timed with a
-512 MB L2 flush between runs.
+decode, the fused attention-input step on a 2,048-token chunk) timed with an
+L2 flush before each run that leaves L2 clean and cold (a 512 MB write, then
+a 512 MB read; the decode lines also give the time after the write alone,
+whose dirty lines the timed launch then writes back).
 `--impl reference` times the fp64 CPU oracle on the host cores instead.
 """
 import argparse
@@ -446,12 +448,29 @@ def time_e2e(torch, pk, mixed, K, first):
 
 # ------------------------------------------------------ other workloads
 
-def time_events(torch, fn, iters=20, warm=5, flush=None):
+class L2Flush:
+    """Evicts a timed launch's inputs from L2 between timed runs: writes a
+    512 MB buffer (four times the 129 MB L2), then reads another 512 MB, so
+    the dirty lines of that write go back to HBM before the timed region
+    instead of inside it (the launch starts on a clean, cold L2, as under
+    ncu's cache control).  flush(clean=False) does the write alone."""
+
+    def __init__(self, torch):
+        self.w = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(128 << 20, dtype=torch.float32, device="cuda")
+
+    def __call__(self, clean=True):
+        self.w.zero_()
+        if clean:
+            self.r.sum()
+
+
+def time_events(torch, fn, iters=20, warm=5, flush=None, clean=True):
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ts = []
     for i in range(iters + warm):
         if flush is not None:
-            flush.zero_()
+            flush(clean)
         s.record()
         fn()
         e.record()
@@ -485,7 +504,7 @@ def time_graph(torch, fn, reps=20):
 
 
 def other_configs(torch, pk, hbm, bf16):
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     res = {}
 
     def decode_entry(name, case, pool, per_pos, smooth=None, graph=False, fused=False):
@@ -500,11 +519,14 @@ def other_configs(torch, pk, hbm, bf16):
         fn = lambda: pk.paged_attn_decode(pool, q, bt, sl, ms, SCALE, k_smooth=w, workspace=ws,
                                           out=out, lse=lse, fused=fused)
         med, mn = time_events(torch, fn, flush=flush)
+        med_w, _ = time_events(torch, fn, flush=flush, clean=False)
         byts = decode_bytes(case.seq_lens, case.Hkv, per_pos)
         r = {"us": round(med, 2), "us_min": round(mn, 2), "GBps": round(byts / med / 1e3, 1),
              "frac_of_8TBps": round(byts / med / 1e3 / NOMINAL_HBM_GBS, 4),
              "frac_of_measured": round(byts / med / 1e3 / hbm, 4), "bytes": int(byts),
-             "splits": S, "cold_l2": True}
+             "splits": S, "cold_l2": "clean",
+             "us_write_only_flush": round(med_w, 2),
+             "frac_of_measured_write_only_flush": round(byts / med_w / 1e3 / hbm, 4)}
         if fused:
             r["note"] = "combine fused into the split kernel (pkv_paged_attn_decode_fused)"
         if graph:
@@ -878,9 +900,9 @@ def profile_case(torch, pk, name, reps=3):
     for _ in range(reps):
         fn()
     torch.cuda.synchronize()
-    # per-launch time with a 512 MB L2 flush before each launch (back-to-back
+    # per-launch time with an L2 flush before each launch (back-to-back
     # launches of a short kernel would time the Python call, not the kernel)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch)
     us, _ = time_events(torch, fn, iters=10, warm=0, flush=flush)
     rate = work / us / (1e6 if unit == "TFLOP/s" else 1e3)
     assert pk.poll_device_error() == pk.OK
