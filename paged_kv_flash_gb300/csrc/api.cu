@@ -89,8 +89,9 @@ pkv_status check_pool(const pkv_pool* pool) {
 // equal work.  Measured on GB300: 64 sequences of 512..8,192 positions and
 // the 32 decode rows of the mixed step (contexts up to 16,384) run best at
 // 64..96 bf16 pages per split, 8 bf16 sequences of 32,768 positions at 64..96;
-// one 32k-position INT8 sequence at 64 INT8 pages, eight of them at 128.  A
-// forced split count S gives C = ceil(pages / S).
+// one 32k-position INT8 sequence with one full wave of CTAs (37 splits of 56
+// pages; 31 splits, 0.8 per slot, were 8 % slower), eight of them at 128
+// pages.  A forced split count S gives C = ceil(pages / S).
 constexpr long long kPlanSlotsNum = 4, kPlanSlotsDen = 5;   // 0.8 CTAs per slot (bf16)
 constexpr long long kPlanMinPages = 8, kPlanMaxPages = 128, kPlanMaxPagesBf16 = 96;
 
@@ -403,7 +404,9 @@ pkv_status pkv_prefill_plan(int32_t* ctas, size_t* workspace_bytes, size_t* zero
 // decode holds N_d SMs with N_d / (SMs - N_d) = t_d / (kOverlapDecodeGain *
 // t_p), t_p and t_d the two calls' times alone on the whole GPU.  On the
 // mixed step (a 26,926-token prompt in 2,048-row chunks beside 32 decode
-// rows) this picks within a few percent of the best of a sweep per chunk.
+// rows) this picks within a few percent of the best of a sweep per chunk,
+// and the factor 2 was the best of 1.6..4.0 (a larger prefill share pushes
+// the decode's CTAs into a further wave).
 constexpr double kOverlapPrefillFlopsPerSec = 1.45e15, kOverlapPrefillFixedSec = 10e-6;
 constexpr double kOverlapDecodeBytesPerSec = 6.5e12, kOverlapDecodeGain = 2.0;
 
