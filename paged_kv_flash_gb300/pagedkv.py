@@ -129,17 +129,42 @@ class Pool:
         return self.k.shape[1]
 
     def c(self) -> _Pool:
-        """The C struct of the pool, rebuilt only when a tensor has changed
-        (it is passed on every call, and a serving loop makes many)."""
+        """The C struct of the pool, rebuilt (and the tensors checked) only
+        when a tensor has changed (it is passed on every call, and a serving
+        loop makes many)."""
         key = (self.k.data_ptr(), self.v.data_ptr(),
                self.k_scale.data_ptr() if self.k_scale is not None else None,
                self.v_scale.data_ptr() if self.v_scale is not None else None,
-               tuple(self.k.shape), self.dtype)
+               tuple(self.k.shape), tuple(self.v.shape), self.k.device, self.dtype)
         cached = self.__dict__.get("_c")
         if cached is None or cached[0] != key:
-            cached = (key, _Pool(key[0], key[1], key[2], key[3], *key[4], key[5]))
+            self._validate()
+            cached = (key, _Pool(key[0], key[1], key[2], key[3], *key[4], key[7]))
             self.__dict__["_c"] = cached
         return cached[1]
+
+    def _validate(self):
+        """The kernels take the pool's pointers as they are: host memory or a
+        wrong layout must be refused here, before any launch."""
+        want = torch.int8 if self.k.dtype == torch.int8 else torch.bfloat16
+        _need(self.k, want, "pool.k")
+        _need(self.v, want, "pool.v")
+        if (self.k.dim() != 4 or tuple(self.k.shape[2:]) != (PAGE_SIZE, HEAD_DIM)
+                or self.v.shape != self.k.shape or self.v.device != self.k.device):
+            raise ValueError(f"pool: k and v must be [num_pages][Hkv][{PAGE_SIZE}][{HEAD_DIM}] "
+                             f"on one device, got {tuple(self.k.shape)} on {self.k.device} "
+                             f"and {tuple(self.v.shape)} on {self.v.device}")
+        scales = (("pool.k_scale", self.k_scale), ("pool.v_scale", self.v_scale))
+        if want == torch.int8:
+            for name, t in scales:
+                if t is None:
+                    raise ValueError(f"{name}: an INT8 pool needs fp32 scales")
+                _need(t, torch.float32, name)
+                if tuple(t.shape) != tuple(self.k.shape[:3]) or t.device != self.k.device:
+                    raise ValueError(f"{name}: expected {tuple(self.k.shape[:3])} on "
+                                     f"{self.k.device}, got {tuple(t.shape)} on {t.device}")
+        elif self.k_scale is not None or self.v_scale is not None:
+            raise ValueError("a bf16 pool has no scales")
 
     @staticmethod
     def empty(num_pages: int, num_kv_heads: int, dtype=torch.bfloat16, device="cuda"):
