@@ -198,9 +198,14 @@ def test_keys_after_the_causal_edge_do_not_matter():
 def _sdpa_reference(q, k, v, scale, qlen, L, G):
     """torch's scaled_dot_product_attention in float64 with a bottom-right
     causal mask, GQA by repeating KV heads; lse via torch.logsumexp."""
-    qt = torch.from_numpy(f(q)).permute(1, 0, 2)                  # [Hq][qlen][D]
-    kt = torch.from_numpy(f(k)).permute(1, 0, 2).repeat_interleave(G, dim=0)
-    vt = torch.from_numpy(f(v)).permute(1, 0, 2).repeat_interleave(G, dim=0)
+    return _sdpa_f64(f(q), f(k), f(v), scale, qlen, L, G)
+
+
+def _sdpa_f64(q, k, v, scale, qlen, L, G):
+    """_sdpa_reference on float64 arrays q [qlen][Hq][D], k, v [L][Hkv][D]."""
+    qt = torch.from_numpy(q).permute(1, 0, 2)                     # [Hq][qlen][D]
+    kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(G, dim=0)
+    vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(G, dim=0)
     i = torch.arange(qlen)[:, None]
     j = torch.arange(L)[None, :]
     mask = j <= (L - qlen + i)
@@ -229,6 +234,60 @@ def test_causal_prefill_matches_sdpa(shape):
         ro, rl = _sdpa_reference(qs[b], ks[b], vs[b], scale, qlen, L, G)
         np.testing.assert_allclose(out[cu[b]:cu[b + 1]], ro, rtol=0, atol=1e-12)
         np.testing.assert_allclose(lse[cu[b]:cu[b + 1]], rl, rtol=0, atol=1e-12)
+
+
+def _int8_cache(rng, shape, Hkv, G, w):
+    """Sequences (qlen, L) of N(0,1) bf16 keys and values quantised into an
+    INT8 cache by the oracle's append (key smoothing w, or None); returns the
+    pools, scales, layout, queries and the bf16 inputs."""
+    ks = [W.normal_bf16(rng, (L, Hkv, D)) for _, L in shape]
+    vs = [W.normal_bf16(rng, (L, Hkv, D)) for _, L in shape]
+    qs = np.concatenate([W.normal_bf16(rng, (qlen, Hkv * G, D)) for qlen, _ in shape])
+    kp, _, bt, lens = make_pool_from_dense(rng, ks, vs)
+    k8, v8, kscale, vscale = W.empty_pool_int8(kp.shape[0], Hkv)
+    k8, v8, kscale, vscale = oracle.kv_append_int8(
+        k8, v8, kscale, vscale, np.concatenate(ks), np.concatenate(vs),
+        W.cu_from_counts([L for _, L in shape]), bt, lens, k_smooth=w)
+    return k8, v8, kscale, vscale, bt, lens, qs
+
+
+def test_int8_attention_matches_sdpa_on_the_dequantised_cache():
+    """Causal rows over an INT8 cache with per-vector scales and key
+    smoothing equal torch's SDPA in float64 on the dequantised vectors, key
+    = code * scale * w and value = code * scale: each scale and the smoothing
+    weight enter once, on their own operand."""
+    rng = np.random.default_rng(31)
+    Hkv, G = 2, 2
+    shape = [(3, 45), (1, 20), (16, 16)]
+    w = rng.uniform(0.5, 2.0, D).astype(np.float32)
+    k8, v8, kscale, vscale, bt, lens, q = _int8_cache(rng, shape, Hkv, G, w)
+    cu = W.cu_from_counts([qlen for qlen, _ in shape])
+    scale = 1 / math.sqrt(D)
+    out, lse = oracle.paged_attention(k8, v8, q, cu, bt, lens, scale, k_scale=kscale,
+                                      v_scale=vscale, k_smooth=w)
+    for b, (qlen, L) in enumerate(shape):
+        pg, sl = bt[b, np.arange(L) // P], np.arange(L) % P
+        kd = (k8[pg, :, sl].astype(np.float64) * kscale[pg, :, sl][:, :, None].astype(np.float64)
+              * w.astype(np.float64))
+        vd = v8[pg, :, sl].astype(np.float64) * vscale[pg, :, sl][:, :, None].astype(np.float64)
+        ro, rl = _sdpa_f64(f(q[cu[b]:cu[b + 1]]), kd, vd, scale, qlen, L, G)
+        np.testing.assert_allclose(out[cu[b]:cu[b + 1]], ro, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[cu[b]:cu[b + 1]], rl, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("S", [2, 5, 13])
+def test_int8_split_plus_combine_equals_unsplit(S):
+    rng = np.random.default_rng(32)
+    Hkv, G = 2, 4
+    shape = [(1, 200), (1, 33), (1, 16), (1, 97)]
+    w = rng.uniform(0.5, 2.0, D).astype(np.float32)
+    k8, v8, kscale, vscale, bt, lens, q = _int8_cache(rng, shape, Hkv, G, w)
+    args = (k8, v8, q, decode_cu(len(shape)), bt, lens, 1 / math.sqrt(D))
+    kw = dict(k_scale=kscale, v_scale=vscale, k_smooth=w)
+    ref, lref = oracle.paged_attention(*args, **kw)
+    out, lse = oracle.paged_attention(*args, num_splits=S, **kw)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lref, rtol=0, atol=1e-12)
 
 
 def test_row_subset_matches_full_evaluation():
