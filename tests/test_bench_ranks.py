@@ -1,6 +1,8 @@
 """The multi-process path of bench.py on CPU (no GPU): with N replicas, one
 process per GPU, the job's time is the slowest rank's (max over ranks), and
-under torchrun only rank 0 runs and prints the reference arm."""
+under torchrun only rank 0 runs and prints the reference arm, whose line
+keeps the GPU arm's metric, unit and config."""
+import json
 import os
 import socket
 import sys
@@ -56,3 +58,24 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--gpus", "2"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """Rank 0 (no torchrun) times the fp64 oracle on a bounded sample of one
+    step and prints one JSON line with the GPU arm's metric, unit and config
+    (about 15 s: the mixed workload is built and one step is sampled)."""
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "1"]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "us" and line["higher_is_better"] is False
+    assert line["steps"] == 1 and line["warmup"] >= 3 and line["n_gpus"] == 1
+    assert line["value"] > 0 and line["ms_per_step"] == pytest.approx(line["value"] / 1e3, rel=1e-3)
+    assert line["dtype"] == "f64" and "mixed continuous-batching step" in line["config"]["workload"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "us", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
